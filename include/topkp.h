@@ -1,0 +1,153 @@
+/*
+ * topkp.h -- C ABI of libtopkp.so, the fused top-k / top-p logit filter for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What it computes.  The operation is the one defined in section 2
+ * (计算流程与公式) of the web page "CANN ops-nn 算子实战：
+ * ApplyTopKTopPWithSorted 的 top-k/top-p 采样过滤原理与 aclnn 调用指南":
+ * per row of a [B, V] logits matrix,
+ *   1. order the row ascending with a stable sort (equal values keep their
+ *      index order; -0 equals +0);
+ *   2. if top-k is on, every value strictly below the k-th largest becomes
+ *      -inf (values equal to the k-th largest survive);
+ *   3. softmax in fp32 over the surviving values;
+ *   4. ascending cumulative sum C_j of those probabilities;
+ *   5. if top-p is on, every sorted position with C_j <= round_D(1 - p)
+ *      becomes -inf, except the last (largest) position, which always stays;
+ *   6. results go back to the original order: each output element is either
+ *      the input element, bit for bit, or the dtype's -inf
+ *      (fp32 0xFF800000, fp16 0xFC00, bf16 0xFF80).
+ * Top-k is on for row b iff k != NULL and 1 <= k[b] <= V-1 (section 4,
+ * 约束说明: k <= 0 or k >= V means no top-k).  Top-p is on iff p != NULL.
+ * round_D(1 - p) is 1 - p evaluated in fp32 and rounded to the logits dtype,
+ * because p has the logits dtype (section 3, 参数说明).
+ *
+ * Results.  Top-k decisions are exact.  A top-p decision can differ from the
+ * exact fp32 definition only at positions whose cumulative probability lies
+ * within about 1e-6 of round_D(1 - p) (the library sums probability mass in
+ * 64-bit fixed point from fp32 exponentials).  Results are deterministic:
+ * the same inputs give the same bits on every call.
+ *
+ * Conventions shared by every entry point.
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     never frees or retains them past the call, and allocates no device
+ *     memory per call.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous: the function returns after the launch is enqueued, and
+ *     no argument check synchronises the device.
+ *   - Row-major layout; V is the fastest-varying dimension.
+ *   - The calling thread's current CUDA device must own the pointers.
+ *   - Value ranges are not checked (the page's CheckParams checks null
+ *     pointers, dtypes and shapes only): p outside [0, 1], NaN or +inf
+ *     logits, an unsorted sorted_value or a sorted_indices that is not a
+ *     permutation give unspecified output; sorted_indices entries outside
+ *     [0, V) are skipped, never written through.
+ *   - On any non-zero status nothing was launched; topkp_last_error_string()
+ *     gives a one-line reason (thread-local, like aclGetRecentErrMsg in
+ *     section 8 of the page).
+ */
+#ifndef TOPKP_H
+#define TOPKP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of logits, p, sorted_value and out (section 3: FLOAT,
+ * FLOAT16, BFLOAT16; p has the same dtype as the logits). */
+typedef enum {
+  TOPKP_F32 = 0,
+  TOPKP_F16 = 1,
+  TOPKP_BF16 = 2
+} topkp_dtype;
+
+typedef int topkp_status;
+
+/* Status codes.  The two parameter errors reuse the page's aclnn codes
+ * (section 5.3 返回码与异常场景). */
+#define TOPKP_SUCCESS 0
+/* logits / sorted_value / sorted_indices / out is NULL on a non-empty
+ * problem, or p and k are both NULL. */
+#define TOPKP_ERR_PARAM_NULLPTR 161001
+/* unknown dtype, B or V negative, V above TOPKP_MAX_V, a row stride below V,
+ * or out overlapping an input without being identical to it. */
+#define TOPKP_ERR_PARAM_INVALID 161002
+/* the CUDA launch failed (including: no CUDA device). */
+#define TOPKP_ERR_LAUNCH 561000
+/* a kernel gave up a bounded wait on its own copy-completion barrier; it
+ * skipped its writes for the affected rows.  Reported by
+ * topkp_device_status(). */
+#define TOPKP_ERR_DEVICE_TIMEOUT 561001
+
+/* Largest supported row length: probability mass is summed in unsigned
+ * 64-bit fixed point with 2^40 per unit, so a row may hold at most 2^23
+ * elements. */
+#define TOPKP_MAX_V (1LL << 23)
+
+/*
+ * topkp_apply -- aclnnApplyTopKTopP (section 5 of the page): filter raw
+ * logits; the ordering is found internally, without a full sort.
+ *
+ *   logits     device, [B, V] of dtype, row stride ld_logits elements (>= V).
+ *   B, V       rows and row length (>= 0).  B == 0 or V == 0 returns
+ *              TOPKP_SUCCESS without a launch.  V == 1 copies the row.
+ *   ld_logits  row stride of logits in elements.
+ *   dtype      TOPKP_F32, TOPKP_F16 or TOPKP_BF16.
+ *   p          device, [B] of dtype, or NULL (top-p off).
+ *   k          device, [B] int32, or NULL (top-k off).  p and k must not both
+ *              be NULL.
+ *   out        device, [B, V] of dtype, row stride ld_out elements (>= V).
+ *              out == logits with ld_out == ld_logits (in place) is allowed;
+ *              any other overlap with logits, p or k is rejected.
+ *   stream     cudaStream_t to launch on.
+ */
+topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_logits,
+                         topkp_dtype dtype, const void* p, const int32_t* k,
+                         void* out, int64_t ld_out, void* stream);
+
+/*
+ * topkp_apply_sorted -- the graph op ApplyTopKTopPWithSorted (section 3 of
+ * the page): the caller supplies each row already sorted.
+ *
+ *   sorted_value    device, [B, V] contiguous, dtype; each row ascending, and
+ *                   equal values in increasing original-index order (the
+ *                   stable sort of section 6.1).
+ *   sorted_indices  device, [B, V] contiguous int32: sorted_value[b][j] came
+ *                   from column sorted_indices[b][j] of the logits.
+ *   B, V, dtype     as for topkp_apply.
+ *   p, k            as for topkp_apply (same top-k disable rule).
+ *   logits          device, [B, V] contiguous, dtype, or NULL.  When given,
+ *                   kept outputs are read from it in original order and only
+ *                   the elements tied with the cut value go through
+ *                   sorted_indices (the page's CompareSelectOnLogits +
+ *                   ScatterBoundary); when NULL, every output is scattered
+ *                   through sorted_indices.
+ *   out             device, [B, V] contiguous, dtype; must not overlap any
+ *                   input.
+ */
+topkp_status topkp_apply_sorted(const void* sorted_value, const int32_t* sorted_indices,
+                                int64_t B, int64_t V, topkp_dtype dtype,
+                                const void* p, const int32_t* k, const void* logits,
+                                void* out, void* stream);
+
+/* One-line description of the last non-zero status returned on the calling
+ * thread ("" if none).  The pointer stays valid until the thread's next call
+ * into the library. */
+const char* topkp_last_error_string(void);
+
+/* Waits for all work on stream, then reports (and clears) the device-side
+ * error word on the current device: TOPKP_SUCCESS, TOPKP_ERR_DEVICE_TIMEOUT,
+ * or TOPKP_ERR_LAUNCH if the stream itself reported a CUDA error. */
+topkp_status topkp_device_status(void* stream);
+
+/* Number of kernel launches the most recent successful topkp_apply /
+ * topkp_apply_sorted call on this thread enqueued (0 for an empty problem). */
+int topkp_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOPKP_H */

@@ -141,6 +141,14 @@ def filter_sorted_row(s: np.ndarray, V: int, k: int | None, thr: np.float32 | No
     return kept, C
 
 
+def topk_survivors(s: np.ndarray, V: int, k: int | None) -> np.ndarray:
+    """Sorted positions that survive steps 1-3 alone (reported to the tests,
+    which must tell a top-k difference -- never allowed -- from a top-p one)."""
+    if not topk_enabled(k, V):
+        return np.ones(V, dtype=bool)
+    return ~(s < s[V - int(k)])
+
+
 def scatter_back(raw_sorted_bits: np.ndarray, idx: np.ndarray, kept: np.ndarray, dtype: str):
     """Step 8 ([guide] §2 golden ``scatter_``; reading R1): out[idx[j]] is the
     sorted element's bits if kept, else the dtype's -inf."""
@@ -155,10 +163,10 @@ def scatter_back(raw_sorted_bits: np.ndarray, idx: np.ndarray, kept: np.ndarray,
 class RowInfo:
     """Per-row intermediate results, kept for the tests' tolerance checks."""
 
-    __slots__ = ("idx", "kept", "C", "thr")
+    __slots__ = ("idx", "kept", "C", "thr", "topk_kept")
 
-    def __init__(self, idx, kept, C, thr):
-        self.idx, self.kept, self.C, self.thr = idx, kept, C, thr
+    def __init__(self, idx, kept, C, thr, topk_kept=None):
+        self.idx, self.kept, self.C, self.thr, self.topk_kept = idx, kept, C, thr, topk_kept
 
 
 def _bits_to_raw(bits: np.ndarray, dtype: str) -> np.ndarray:
@@ -179,7 +187,7 @@ def apply_row(x_raw: np.ndarray, dtype: str, p_raw=None, k=None):
     thr = None if p_raw is None else top_p_threshold(p_raw, dtype)
     kept, C = filter_sorted_row(s, V, k, thr)
     out_bits = scatter_back(bits[idx], idx, kept, dtype)
-    return _bits_to_raw(out_bits, dtype), RowInfo(idx, kept, C, thr)
+    return _bits_to_raw(out_bits, dtype), RowInfo(idx, kept, C, thr, topk_survivors(s, V, k))
 
 
 def apply_sorted_row(sv_raw: np.ndarray, si: np.ndarray, dtype: str, p_raw=None, k=None):
@@ -193,7 +201,7 @@ def apply_sorted_row(sv_raw: np.ndarray, si: np.ndarray, dtype: str, p_raw=None,
     thr = None if p_raw is None else top_p_threshold(p_raw, dtype)
     kept, C = filter_sorted_row(s, V, k, thr)
     out_bits = scatter_back(raw_bits(sv_raw, dtype), idx, kept, dtype)
-    return _bits_to_raw(out_bits, dtype), RowInfo(idx, kept, C, thr)
+    return _bits_to_raw(out_bits, dtype), RowInfo(idx, kept, C, thr, topk_survivors(s, V, k))
 
 
 def apply(x_raw: np.ndarray, dtype: str, p_raw=None, k=None, rows=None):

@@ -1,0 +1,106 @@
+"""The C ABI without a GPU: the library builds, loads, exports every entry
+point that include/topkp.h declares, and rejects bad arguments with the
+page's status codes before touching the device (section 5.3 of the CANN
+ops-nn ApplyTopKTopPWithSorted guide: 161001 null pointer, 161002 invalid)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "topkp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from top_logit_filter_gb300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(topkp_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_expected_calls():
+    assert _declared() == sorted(["topkp_apply", "topkp_apply_sorted", "topkp_last_error_string",
+                                  "topkp_device_status", "topkp_last_launch_count"])
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(os.path.join(ROOT, "top_logit_filter_gb300", "libtopkp.so"))
+    for name in _declared():
+        assert hasattr(raw, name), name
+
+
+def test_binding_names_every_export():
+    from top_logit_filter_gb300 import _lib
+    assert sorted(_lib.EXPORTS) == _declared()
+
+
+F32, F16, BF16 = 0, 1, 2
+NULLPTR, INVALID, LAUNCH = 161001, 161002, 561000
+FAKE = 1 << 20  # never dereferenced: every check below fails before a launch
+
+
+def _apply(lib, x=FAKE, B=2, V=8, ldx=None, dt=F32, p=None, k=FAKE + 4096, out=FAKE + 8192, ldo=None):
+    return lib.topkp_apply(x, B, V, V if ldx is None else ldx, dt, p, k, out, V if ldo is None else ldo, None)
+
+
+def test_apply_argument_errors(lib):
+    assert _apply(lib, p=None, k=None) == NULLPTR
+    assert b"both NULL" in lib.topkp_last_error_string()
+    assert _apply(lib, dt=7) == INVALID
+    assert _apply(lib, B=-1) == INVALID
+    assert _apply(lib, V=-3) == INVALID
+    assert _apply(lib, V=(1 << 23) + 1) == INVALID
+    assert _apply(lib, x=None) == NULLPTR
+    assert _apply(lib, out=None) == NULLPTR
+    assert _apply(lib, ldx=7) == INVALID
+    assert _apply(lib, ldo=4) == INVALID
+    # out overlapping logits without being the same buffer
+    assert _apply(lib, x=FAKE, out=FAKE + 4) == INVALID
+    assert _apply(lib, x=FAKE, out=FAKE, ldx=8, ldo=9) == INVALID
+    # out overlapping k or p
+    assert _apply(lib, k=FAKE + 8192, out=FAKE + 8192 - 4) == INVALID
+    assert _apply(lib, p=FAKE + 8200, k=None) == INVALID
+
+
+def test_apply_empty_problems_succeed_without_launch(lib):
+    assert _apply(lib, B=0) == 0
+    assert _apply(lib, V=0, x=None, out=None) == 0
+    assert lib.topkp_last_launch_count() == 0
+
+
+def test_sorted_argument_errors(lib):
+    def call(sv=FAKE, si=FAKE + 4096, B=2, V=8, dt=BF16, p=FAKE + 12000, k=None, lg=None, out=FAKE + 8192):
+        return lib.topkp_apply_sorted(sv, si, B, V, dt, p, k, lg, out, None)
+    assert call(p=None, k=None) == NULLPTR
+    assert call(dt=3) == INVALID
+    assert call(B=-2) == INVALID
+    assert call(sv=None) == NULLPTR
+    assert call(si=None) == NULLPTR
+    assert call(out=None) == NULLPTR
+    assert call(out=FAKE + 8) == INVALID          # overlaps sorted_value
+    assert call(lg=FAKE + 8190) == INVALID        # overlaps out
+    assert call(B=0) == 0
+
+
+def test_no_device_fails_loudly_instead_of_falling_back(lib):
+    """Valid arguments but no usable GPU: the call must report a launch error
+    (there is no CPU path)."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _apply(lib) == LAUNCH
+    assert b"device" in lib.topkp_last_error_string()
+
+
+def test_python_binding_rejects_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    import top_logit_filter_gb300 as tk
+    with pytest.raises(ValueError):
+        tk.apply(torch.zeros(2, 8), k=torch.ones(2, dtype=torch.int32))

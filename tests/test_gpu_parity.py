@@ -1,0 +1,182 @@
+"""GPU parity: libtopkp.so (through the C ABI) against the CPU oracle.
+
+Small cases sweep dtypes, ragged row lengths, every launch plan, the k / p
+edge values of sections 4 and 2 of the CANN ops-nn ApplyTopKTopPWithSorted
+guide, tie-heavy rows, signed zeros, strided, unaligned and in-place buffers.
+The five workloads then run at full size, in the launch configuration the
+benchmark uses, checked row by row on a sample (and by closed forms on every
+row where one exists)."""
+import numpy as np
+import pytest
+
+import oracle as O
+from parity import compare_row
+from rawutil import NEG_INF, bits, raw_to_torch, to_raw, torch_to_raw
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DTS = ("f32", "f16", "bf16")
+
+
+@pytest.fixture(scope="module")
+def tk():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from top_logit_filter_gb300 import build
+    build.build()
+    import top_logit_filter_gb300 as m
+    return m
+
+
+def _rows(rng, B, V, dtype, kind):
+    if kind == "normal":
+        x = rng.standard_normal((B, V)).astype(np.float32) * 3
+    elif kind == "ties":
+        x = (rng.integers(-6, 7, size=(B, V)) * 0.5).astype(np.float32)
+    else:  # "zeros": signed zeros and a few values
+        x = rng.choice(np.array([-0.0, 0.0, 1.0, -1.0, 2.0], dtype=np.float32), size=(B, V))
+    return np.stack([to_raw(r, dtype) for r in x])
+
+
+def _kp(rng, B, V, dtype, mode):
+    kcand = [-1, 0, 1, 2, max(1, V // 3), V - 1, V, V + 5, int(rng.integers(1, max(2, V)))]
+    pcand = [0.0, 0.3, 0.9, 1.0, float(rng.random()), 0.5]
+    k = np.array([kcand[i % len(kcand)] for i in range(B)], dtype=np.int32) if mode != "p" else None
+    p = to_raw([pcand[i % len(pcand)] for i in range(B)], dtype) if mode != "k" else None
+    return k, p
+
+
+def _run_apply(tk, x, dtype, p, k, out=None):
+    xt = raw_to_torch(x, dtype, "cuda")
+    pt = None if p is None else raw_to_torch(p, dtype, "cuda")
+    kt = None if k is None else torch.from_numpy(k).cuda()
+    o = tk.apply(xt, p=pt, k=kt, out=out)
+    torch.cuda.synchronize()
+    return torch_to_raw(o, dtype)
+
+
+def _check_all(out, x, dtype, p, k, where):
+    flips = 0
+    for b in range(x.shape[0]):
+        _, info = O.apply_row(x[b], dtype, None if p is None else p[b], None if k is None else int(k[b]))
+        flips += compare_row(out[b], x[b], info, dtype, where=f"{where} row {b}")
+    return flips
+
+
+PLANS = ["", "1,1", "2,1", "3,1", "4,0", "5,1", "8,1", "2,0"]
+
+
+@pytest.mark.parametrize("dtype", DTS)
+@pytest.mark.parametrize("V", [1, 2, 7, 64, 1000, 5003])
+@pytest.mark.parametrize("mode", ["k", "p", "kp"])
+def test_small_rows_all_plans(tk, monkeypatch, dtype, V, mode):
+    rng = np.random.default_rng(V * 7 + len(mode))
+    B = 9
+    for kind in ("normal", "ties", "zeros"):
+        x = _rows(rng, B, V, dtype, kind)
+        k, p = _kp(rng, B, V, dtype, mode)
+        for plan in PLANS:
+            monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
+            out = _run_apply(tk, x, dtype, p, k)
+            _check_all(out, x, dtype, p, k, f"{dtype} V={V} {mode} {kind} plan={plan!r}")
+
+
+@pytest.mark.parametrize("dtype", DTS)
+def test_multi_slice_rows(tk, monkeypatch, dtype):
+    """Rows long enough that every CTA of a cluster holds several vectors and
+    a ragged last slice."""
+    rng = np.random.default_rng(3)
+    B, V = 6, 40011
+    for kind in ("normal", "ties"):
+        x = _rows(rng, B, V, dtype, kind)
+        k, p = _kp(rng, B, V, dtype, "kp")
+        k[:3] = [0, 37, 900]
+        for plan in ("", "1,1", "4,1", "7,1", "16,1", "8,0"):
+            monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
+            out = _run_apply(tk, x, dtype, p, k)
+            _check_all(out, x, dtype, p, k, f"{dtype} {kind} plan={plan!r}")
+
+
+@pytest.mark.parametrize("dtype", DTS)
+def test_strided_unaligned_and_in_place(tk, dtype):
+    rng = np.random.default_rng(11)
+    B, V = 5, 3001
+    x = _rows(rng, B, V, dtype, "normal")
+    k, p = _kp(rng, B, V, dtype, "kp")
+    pt = raw_to_torch(p, dtype, "cuda")
+    kt = torch.from_numpy(k).cuda()
+    big = torch.zeros((B, V + 9), dtype=raw_to_torch(x, dtype).dtype, device="cuda")
+    big[:, 1:V + 1] = raw_to_torch(x, dtype, "cuda")       # misaligned base, stride V+9
+    view = big[:, 1:V + 1]
+    obig = torch.zeros_like(big)
+    out = tk.apply(view, p=pt, k=kt, out=obig[:, 3:V + 3])
+    torch.cuda.synchronize()
+    _check_all(torch_to_raw(out, dtype), x, dtype, p, k, f"{dtype} strided")
+    # untouched padding
+    assert torch.count_nonzero(obig[:, :3]) == 0 and torch.count_nonzero(obig[:, V + 3:]) == 0
+    # in place
+    xt = raw_to_torch(x, dtype, "cuda")
+    r = tk.apply(xt, p=pt, k=kt, out=xt)
+    torch.cuda.synchronize()
+    assert r.data_ptr() == xt.data_ptr()
+    _check_all(torch_to_raw(xt, dtype), x, dtype, p, k, f"{dtype} in place")
+
+
+def test_empty_and_single_column(tk):
+    x = torch.zeros((0, 5), device="cuda")
+    assert tk.apply(x, k=torch.zeros(0, dtype=torch.int32, device="cuda")).shape == (0, 5)
+    x = torch.zeros((3, 0), device="cuda")
+    assert tk.apply(x, k=torch.ones(3, dtype=torch.int32, device="cuda")).shape == (3, 0)
+    x = torch.tensor([[-1.5], [2.0], [0.0]], device="cuda")
+    o = tk.apply(x, p=torch.tensor([0.0, 0.5, 1.0], device="cuda"), k=torch.ones(3, dtype=torch.int32, device="cuda"))
+    assert torch.equal(o, x)
+
+
+def test_deterministic(tk):
+    from top_logit_filter_gb300 import workloads
+    w = workloads.make(3, B=32)
+    xt = raw_to_torch(w["x"], "bf16", "cuda")
+    pt = raw_to_torch(w["p"], "bf16", "cuda")
+    kt = torch.from_numpy(w["k"]).cuda()
+    a = tk.apply(xt, p=pt, k=kt)
+    for _ in range(3):
+        b = tk.apply(xt, p=pt, k=kt)
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    tk.device_status()
+
+
+# ------------------------------------------------------------ full workloads
+def _workload_inputs(w):
+    dt = w["dtype"]
+    xt = raw_to_torch(w["x"], dt, "cuda")
+    pt = None if w["p"] is None else raw_to_torch(w["p"], dt, "cuda")
+    kt = None if w["k"] is None else torch.from_numpy(w["k"]).cuda()
+    return xt, pt, kt
+
+
+@pytest.mark.parametrize("wl,sample", [(1, None), (2, None), (3, None), (4, 48)])
+def test_workload_full_size(tk, wl, sample):
+    from top_logit_filter_gb300 import workloads
+    w = workloads.make(wl)
+    dt = w["dtype"]
+    xt, pt, kt = _workload_inputs(w)
+    out = torch_to_raw(tk.apply(xt, p=pt, k=kt), dt)
+    tk.device_status()
+    B = w["B"]
+    rows = range(B) if sample is None else np.random.default_rng(wl).choice(B, sample, replace=False)
+    flips = 0
+    for b in rows:
+        _, info = O.apply_row(w["x"][b], dt, None if w["p"] is None else w["p"][b],
+                              None if w["k"] is None else int(w["k"][b]))
+        flips += compare_row(out[b], w["x"][b], info, dt, where=f"workload {wl} row {b}")
+    print(f"workload {wl}: {len(rows)} rows checked, {flips} top-p flips inside the band")
+    if wl == 4:
+        # top-k alone on every row: out == where(x >= k-th largest, x, -inf)
+        xv = O.decode(w["x"], dt)
+        ob = bits(out, dt)
+        for b in range(B):
+            kk = int(w["k"][b])
+            kth = np.partition(xv[b], w["V"] - kk)[w["V"] - kk]
+            exp = np.where(xv[b] >= kth, bits(w["x"][b], dt), NEG_INF[dt])
+            assert np.array_equal(ob[b], exp), f"row {b}"

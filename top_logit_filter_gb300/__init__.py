@@ -1,0 +1,138 @@
+"""GB300-native fused top-k / top-p logit filter.
+
+Python face of libtopkp.so (include/topkp.h).  This module only marshals
+arguments: every step of the filter runs in the library's CUDA kernels, and
+there is no CPU path -- without the built library, or without a CUDA tensor,
+the calls raise.
+
+    out = apply(logits, p=None, k=None, out=None)
+    out = apply_sorted(sorted_value, sorted_indices, p=None, k=None, logits=None, out=None)
+
+Semantics: section 2 of the web page "CANN ops-nn 算子实战：
+ApplyTopKTopPWithSorted 的 top-k/top-p 采样过滤原理与 aclnn 调用指南" --
+per row, values strictly below the k-th largest become -inf, then sorted
+positions whose fp32 cumulative softmax probability is <= 1-p become -inf
+(never the largest), and every other element keeps its bits.
+"""
+from __future__ import annotations
+
+from . import _lib
+from ._lib import (TOPKP_ERR_DEVICE_TIMEOUT, TOPKP_ERR_LAUNCH, TOPKP_ERR_PARAM_INVALID,  # noqa: F401
+                   TOPKP_ERR_PARAM_NULLPTR, TOPKP_MAX_V, TOPKP_SUCCESS)
+
+
+class TopKPError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"[{status}] {message}")
+        self.status = status
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    codes = {torch.float32: _lib.TOPKP_F32, torch.float16: _lib.TOPKP_F16, torch.bfloat16: _lib.TOPKP_BF16}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype} (float32, float16 or bfloat16)")
+    return codes[t.dtype]
+
+
+def _check(status: int):
+    if status != _lib.TOPKP_SUCCESS:
+        raise TopKPError(status, _lib.last_error())
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device):
+    return _torch().cuda.current_stream(device).cuda_stream
+
+
+def _vec(t, n, dtype, name, device):
+    torch = _torch()
+    if t is None:
+        return None
+    if not torch.is_tensor(t):
+        t = torch.as_tensor(t, dtype=dtype, device=device)
+    if t.device != device or t.dtype != dtype or t.dim() != 1 or t.shape[0] != n:
+        raise ValueError(f"{name} must be a 1-D {dtype} tensor of length {n} on {device}")
+    return t.contiguous()
+
+
+def apply(logits, p=None, k=None, out=None):
+    """aclnnApplyTopKTopP: filter a [B, V] CUDA tensor of logits.
+
+    p: [B] tensor of the logits dtype (or None); k: [B] int32 (or None); at
+    least one is required.  Rows may be strided along B (stride(1) must be
+    1).  Returns ``out`` (allocated when None; may be ``logits`` itself)."""
+    torch = _torch()
+    lib = _lib.load()
+    if not torch.is_tensor(logits) or logits.dim() != 2 or not logits.is_cuda:
+        raise ValueError("logits must be a 2-D CUDA tensor")
+    dt = _dtype_code(logits)
+    if logits.stride(1) != 1:
+        logits = logits.contiguous()
+    B, V = logits.shape
+    dev = logits.device
+    p = _vec(p, B, logits.dtype, "p", dev)
+    k = _vec(k, B, torch.int32, "k", dev)
+    if out is None:
+        out = torch.empty((B, V), dtype=logits.dtype, device=dev)
+    if out.shape != logits.shape or out.dtype != logits.dtype or out.device != dev or out.stride(1) != 1:
+        raise ValueError("out must match logits in shape, dtype and device, with stride(1) == 1")
+    with torch.cuda.device(dev):
+        _check(lib.topkp_apply(_ptr(logits), B, V, logits.stride(0) if B > 1 else V, dt, _ptr(p), _ptr(k),
+                               _ptr(out), out.stride(0) if B > 1 else V, _stream(dev)))
+    return out
+
+
+def apply_sorted(sorted_value, sorted_indices, p=None, k=None, logits=None, out=None):
+    """ApplyTopKTopPWithSorted: filter pre-sorted rows.
+
+    sorted_value: [B, V] ascending per row (stable order); sorted_indices:
+    [B, V] int32 source columns; logits (optional): the unsorted rows."""
+    torch = _torch()
+    lib = _lib.load()
+    for name, t in (("sorted_value", sorted_value), ("sorted_indices", sorted_indices)):
+        if not torch.is_tensor(t) or t.dim() != 2 or not t.is_cuda:
+            raise ValueError(f"{name} must be a 2-D CUDA tensor")
+    dt = _dtype_code(sorted_value)
+    B, V = sorted_value.shape
+    dev = sorted_value.device
+    if sorted_indices.shape != (B, V) or sorted_indices.dtype != torch.int32 or sorted_indices.device != dev:
+        raise ValueError("sorted_indices must be an int32 tensor shaped like sorted_value")
+    sorted_value = sorted_value.contiguous()
+    sorted_indices = sorted_indices.contiguous()
+    if logits is not None:
+        if logits.shape != (B, V) or logits.dtype != sorted_value.dtype or logits.device != dev:
+            raise ValueError("logits must match sorted_value in shape, dtype and device")
+        logits = logits.contiguous()
+    p = _vec(p, B, sorted_value.dtype, "p", dev)
+    k = _vec(k, B, torch.int32, "k", dev)
+    if out is None:
+        out = torch.empty((B, V), dtype=sorted_value.dtype, device=dev)
+    if out.shape != (B, V) or out.dtype != sorted_value.dtype or out.device != dev or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like sorted_value")
+    with torch.cuda.device(dev):
+        _check(lib.topkp_apply_sorted(_ptr(sorted_value), _ptr(sorted_indices), B, V, dt, _ptr(p), _ptr(k),
+                                      _ptr(logits), _ptr(out), _stream(dev)))
+    return out
+
+
+def device_status(device=None) -> None:
+    """Synchronises the current stream and raises if a kernel gave up a
+    bounded wait since the last check."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(_lib.load().topkp_device_status(_stream(dev)))
+
+
+def last_launch_count() -> int:
+    """Kernel launches enqueued by the most recent successful call."""
+    return _lib.load().topkp_last_launch_count()

@@ -1,0 +1,299 @@
+// C ABI of libtopkp.so: argument checks (host only, no device sync), launch
+// planning and launches.  The checks follow the order of the page's
+// CheckParams ([guide] §5.3): null pointers, then dtypes, then shapes.
+#include <cstdarg>
+#include <climits>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+#include "internal.h"
+
+namespace topkp {
+namespace {
+
+thread_local std::string g_last_error;
+thread_local int g_last_launches = 0;
+
+topkp_status fail(topkp_status code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+topkp_status fail(topkp_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int esize_of(topkp_dtype dt) {
+  switch (dt) {
+    case TOPKP_F32: return 4;
+    case TOPKP_F16: return 2;
+    case TOPKP_BF16: return 2;
+  }
+  return 0;
+}
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+  if (!a || !b || an == 0 || bn == 0) return false;
+  const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+// Streaming multiprocessor count of the current device (cached per device).
+int current_sms(int* dev_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev]) {
+    *dev_out = dev;
+    return cache[dev];
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (dev >= 0 && dev < 64) cache[dev] = sms;
+  *dev_out = dev;
+  return sms;
+}
+
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s for any single bounded wait
+
+}  // namespace
+
+// ------------------------------------------------------------------ planners
+static int slice_for(int64_t V, int C) {
+  const int64_t s = (V + C - 1) / C;
+  return (int)((s + 15) / 16 * 16);
+}
+
+ApplyPlan plan_apply(int64_t B, int64_t V, int esize, int num_sms, const char* force) {
+  ApplyPlan p;
+  if (force && *force) {
+    int c = 1, st = 1;
+    if (sscanf(force, "%d,%d", &c, &st) >= 1) {
+      c = c < 1 ? 1 : (c > 16 ? 16 : c);
+      while (c > 1 && (int64_t)(c - 1) * slice_for(V, c) >= V) --c;
+      p.csize = c;
+      p.slice = slice_for(V, c);
+      p.staged = st != 0;
+      p.smem = apply_smem_bytes(p.slice, esize, p.staged);
+      if (p.smem <= 227 * 1024) return p;
+    }
+  }
+  // Prefer two CTAs per SM (<= 110 KB each), then one per SM, up to 16 CTAs
+  // per row; beyond that, re-read the row from global memory (L2).
+  const size_t budgets[2] = {110 * 1024, 227 * 1024};
+  const int cmax[2] = {8, 16};
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int c = 1; c <= cmax[pass]; ++c) {
+      const int s = slice_for(V, c);
+      if (c > 1 && (int64_t)(c - 1) * s >= V) break;
+      if (apply_smem_bytes(s, esize, true) <= budgets[pass]) {
+        p.csize = c;
+        p.slice = s;
+        p.staged = true;
+        // few rows: spread each row over more SMs
+        while (p.csize < 8 && B * p.csize < 2LL * num_sms) {
+          const int s2 = slice_for(V, p.csize + 1);
+          if (s2 < 2048 || (int64_t)p.csize * s2 >= V) break;
+          ++p.csize;
+          p.slice = s2;
+        }
+        p.smem = apply_smem_bytes(p.slice, esize, true);
+        return p;
+      }
+    }
+  }
+  p.csize = 8;
+  p.slice = slice_for(V, 8);
+  p.staged = false;
+  p.smem = apply_smem_bytes(p.slice, esize, false);
+  return p;
+}
+
+SortedPlan plan_sorted(int64_t B, int64_t V, int esize, int num_sms, bool with_logits, const char* force) {
+  SortedPlan p;
+  int c = 0;
+  if (force && *force) sscanf(force, "%d", &c);
+  if (c <= 0) {
+    // about 48 KB of logits per CTA, at least two CTAs per SM overall
+    const int64_t bytes = V * esize;
+    c = (int)((bytes + 48 * 1024 - 1) / (48 * 1024));
+    if (c < 1) c = 1;
+    while (c < 8 && B * c < 2LL * num_sms && V / (c + 1) >= 2048) ++c;
+  }
+  if (c > 8) c = 8;
+  while (c > 1 && (int64_t)(c - 1) * slice_for(V, c) >= V) --c;
+  p.csize = c;
+  p.chunk = slice_for(V, c);
+  p.smem = kSortedHdrBytes + (with_logits ? ((size_t)p.chunk * esize + 127) / 128 * 128 : 0);
+  if (p.smem > 227 * 1024) {  // very long rows: no staging
+    p.smem = kSortedHdrBytes;
+  }
+  return p;
+}
+
+}  // namespace topkp
+
+using namespace topkp;
+
+extern "C" {
+
+const char* topkp_last_error_string(void) { return g_last_error.c_str(); }
+
+int topkp_last_launch_count(void) { return g_last_launches; }
+
+topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_logits, topkp_dtype dtype,
+                         const void* p, const int32_t* k, void* out, int64_t ld_out, void* stream) {
+  g_last_launches = 0;
+  if (!p && !k) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_apply: p and k are both NULL (at least one is required)");
+  const int es = esize_of(dtype);
+  if (!es) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: unknown dtype %d", (int)dtype);
+  if (B < 0 || V < 0) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: negative shape B=%lld V=%lld", (long long)B, (long long)V);
+  if (V > TOPKP_MAX_V) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: V=%lld exceeds the maximum %lld", (long long)V, (long long)TOPKP_MAX_V);
+  if (B == 0 || V == 0) return TOPKP_SUCCESS;
+  if (!logits) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_apply: logits is NULL");
+  if (!out) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_apply: out is NULL");
+  if (ld_logits < V || ld_out < V)
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: row stride below V (ld_logits=%lld ld_out=%lld V=%lld)",
+                (long long)ld_logits, (long long)ld_out, (long long)V);
+  const size_t xbytes = (size_t)((B - 1) * ld_logits + V) * es;
+  const size_t obytes = (size_t)((B - 1) * ld_out + V) * es;
+  const bool in_place = (logits == out && ld_logits == ld_out);
+  if (!in_place && overlaps(logits, xbytes, out, obytes))
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: out partially overlaps logits");
+  if (overlaps(p, (size_t)B * es, out, obytes) || overlaps(k, (size_t)B * 4, out, obytes))
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: out overlaps p or k");
+
+  int dev = 0;
+  const int sms = current_sms(&dev);
+  if (sms <= 0) return fail(TOPKP_ERR_LAUNCH, "topkp_apply: no usable CUDA device");
+  const ApplyPlan plan = plan_apply(B, V, es, sms, getenv("TOPKP_FORCE_PLAN"));
+
+  ApplyArgs a = {};
+  a.x = logits;
+  a.out = out;
+  a.p = p;
+  a.k = k;
+  a.ldx = ld_logits;
+  a.ldo = ld_out;
+  a.V = (int32_t)V;
+  a.slice = plan.slice;
+  a.csize = plan.csize;
+  a.bulk_in = ((uintptr_t)logits % 16 == 0) && ((ld_logits * es) % 16 == 0);
+  a.vec_out = ((uintptr_t)out % 16 == 0) && ((ld_out * es) % 16 == 0);
+  a.timeout_ns = kTimeoutNs;
+  // grid.x = rows * csize must stay below 2^31
+  const int64_t max_rows = (INT_MAX / plan.csize);
+  int launches = 0;
+  for (int64_t r0 = 0; r0 < B; r0 += max_rows) {
+    const int64_t nb = B - r0 < max_rows ? B - r0 : max_rows;
+    ApplyArgs ai = a;
+    ai.B = nb;
+    ai.x = (const char*)logits + r0 * ld_logits * es;
+    ai.out = (char*)out + r0 * ld_out * es;
+    ai.p = p ? (const char*)p + r0 * es : nullptr;
+    ai.k = k ? k + r0 : nullptr;
+    const cudaError_t e = launch_apply(dtype, plan, ai, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(TOPKP_ERR_LAUNCH, "topkp_apply: launch failed (%s; csize=%d slice=%d smem=%zu)", cudaGetErrorString(e),
+                  plan.csize, plan.slice, plan.smem);
+    }
+    ++launches;
+  }
+  g_last_launches = launches;
+  return TOPKP_SUCCESS;
+}
+
+topkp_status topkp_apply_sorted(const void* sorted_value, const int32_t* sorted_indices, int64_t B, int64_t V,
+                                topkp_dtype dtype, const void* p, const int32_t* k, const void* logits, void* out,
+                                void* stream) {
+  g_last_launches = 0;
+  if (!p && !k)
+    return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_apply_sorted: p and k are both NULL (at least one is required)");
+  const int es = esize_of(dtype);
+  if (!es) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply_sorted: unknown dtype %d", (int)dtype);
+  if (B < 0 || V < 0)
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply_sorted: negative shape B=%lld V=%lld", (long long)B, (long long)V);
+  if (V > TOPKP_MAX_V)
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply_sorted: V=%lld exceeds the maximum %lld", (long long)V,
+                (long long)TOPKP_MAX_V);
+  if (B == 0 || V == 0) return TOPKP_SUCCESS;
+  if (!sorted_value) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_apply_sorted: sorted_value is NULL");
+  if (!sorted_indices) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_apply_sorted: sorted_indices is NULL");
+  if (!out) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_apply_sorted: out is NULL");
+  const size_t n = (size_t)(B * V);
+  if (overlaps(out, n * es, sorted_value, n * es) || overlaps(out, n * es, sorted_indices, n * 4) ||
+      overlaps(out, n * es, logits, n * es) || overlaps(out, n * es, p, (size_t)B * es) ||
+      overlaps(out, n * es, k, (size_t)B * 4))
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply_sorted: out overlaps an input");
+
+  int dev = 0;
+  const int sms = current_sms(&dev);
+  if (sms <= 0) return fail(TOPKP_ERR_LAUNCH, "topkp_apply_sorted: no usable CUDA device");
+  const SortedPlan plan = plan_sorted(B, V, es, sms, logits != nullptr, getenv("TOPKP_FORCE_SORTED_PLAN"));
+
+  SortedArgs a = {};
+  a.sv = sorted_value;
+  a.si = sorted_indices;
+  a.logits = logits;
+  a.out = out;
+  a.p = p;
+  a.k = k;
+  a.V = (int32_t)V;
+  a.chunk = plan.chunk;
+  a.csize = plan.csize;
+  a.aligned = logits && plan.smem > kSortedHdrBytes && ((uintptr_t)logits % 16 == 0) && ((uintptr_t)out % 16 == 0) &&
+              ((V * es) % 16 == 0);
+  a.timeout_ns = kTimeoutNs;
+  const int64_t max_rows = (INT_MAX / plan.csize);
+  int launches = 0;
+  for (int64_t r0 = 0; r0 < B; r0 += max_rows) {
+    const int64_t nb = B - r0 < max_rows ? B - r0 : max_rows;
+    SortedArgs ai = a;
+    ai.B = nb;
+    ai.sv = (const char*)sorted_value + r0 * V * es;
+    ai.si = sorted_indices + r0 * V;
+    ai.logits = logits ? (const char*)logits + r0 * V * es : nullptr;
+    ai.out = (char*)out + r0 * V * es;
+    ai.p = p ? (const char*)p + r0 * es : nullptr;
+    ai.k = k ? k + r0 : nullptr;
+    const cudaError_t e = launch_sorted(dtype, plan, ai, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(TOPKP_ERR_LAUNCH, "topkp_apply_sorted: launch failed (%s; csize=%d chunk=%d smem=%zu)",
+                  cudaGetErrorString(e), plan.csize, plan.chunk, plan.smem);
+    }
+    ++launches;
+  }
+  g_last_launches = launches;
+  return TOPKP_SUCCESS;
+}
+
+topkp_status topkp_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(TOPKP_ERR_LAUNCH, "topkp_device_status: stream error: %s", cudaGetErrorString(e));
+  }
+  unsigned int w1 = 0, w2 = 0;
+  e = apply_take_device_error(&w1);
+  if (e == cudaSuccess) e = sorted_take_device_error(&w2);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(TOPKP_ERR_LAUNCH, "topkp_device_status: cannot read the device error word: %s", cudaGetErrorString(e));
+  }
+  if (w1 | w2) return fail(TOPKP_ERR_DEVICE_TIMEOUT, "topkp_device_status: a kernel gave up a bounded wait");
+  return TOPKP_SUCCESS;
+}
+
+}  // extern "C"

@@ -1,0 +1,239 @@
+// Device helpers shared by the filter kernels: dtype traits and order keys,
+// PTX wrappers for mbarriers, 1-D bulk (TMA) copies, thread-block-cluster
+// barriers and distributed shared memory, and block-wide scans.
+//
+// Citations "[guide] §N" refer to the web page "CANN ops-nn 算子实战：
+// ApplyTopKTopPWithSorted 的 top-k/top-p 采样过滤原理与 aclnn 调用指南" by
+// its numbered sections.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/topkp.h"
+
+namespace topkp {
+
+constexpr int kThreads = 512;            // threads per CTA in every filter kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kL1Bits = 11;              // first radix digit: 2048 buckets
+constexpr int kL1Bins = 1 << kL1Bits;
+constexpr double kMassScale = 1099511627776.0;  // 2^40 fixed-point units per unit of probability mass
+constexpr float kMassScaleF = 1099511627776.0f;
+
+
+// ------------------------------------------------------------------ dtypes
+// -inf bit patterns of [guide] §6.3 (FLOAT16_NEG_INF, BF16_NEG_INF,
+// FLOAT32_NEG_INF).
+template <int DT> struct DType;
+template <> struct DType<TOPKP_F32> {
+  using raw = uint32_t;
+  static constexpr int kKeyBits = 32;
+  static constexpr raw kNegInf = 0xFF800000u;
+  __device__ static __forceinline__ float to_float(raw b) { return __uint_as_float(b); }
+  __device__ static __forceinline__ float round_to(float v) { return v; }
+};
+template <> struct DType<TOPKP_F16> {
+  using raw = uint16_t;
+  static constexpr int kKeyBits = 16;
+  static constexpr raw kNegInf = 0xFC00u;
+  __device__ static __forceinline__ float to_float(raw b) { return __half2float(__ushort_as_half(b)); }
+  __device__ static __forceinline__ float round_to(float v) { return __half2float(__float2half_rn(v)); }
+};
+template <> struct DType<TOPKP_BF16> {
+  using raw = uint16_t;
+  static constexpr int kKeyBits = 16;
+  static constexpr raw kNegInf = 0xFF80u;
+  __device__ static __forceinline__ float to_float(raw b) { return __uint_as_float(((uint32_t)b) << 16); }
+  __device__ static __forceinline__ float round_to(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+};
+
+// Order key: an unsigned integer whose order is the float order of the
+// value, with -0 and +0 mapped to the same key (the stable sort of
+// [guide] §6.1 treats them as equal).  key = H + |x| for x >= 0 and
+// H - |x| for x < 0, H = 2^(bits-1), on the magnitude bits.
+template <int DT>
+__device__ __forceinline__ uint32_t order_key(typename DType<DT>::raw b) {
+  constexpr uint32_t H = 1u << (DType<DT>::kKeyBits - 1);
+  const uint32_t u = (uint32_t)b;
+  const uint32_t mag = u & (H - 1u);
+  return (u & H) ? (H - mag) : (H + mag);
+}
+
+// Inverse of order_key (canonical +0 for the zero key).
+template <int DT>
+__device__ __forceinline__ typename DType<DT>::raw raw_of_key(uint32_t key) {
+  constexpr uint32_t H = 1u << (DType<DT>::kKeyBits - 1);
+  return (typename DType<DT>::raw)(key >= H ? (key - H) : (H | (H - key)));
+}
+
+template <int DT>
+__device__ __forceinline__ float value_of_key(uint32_t key) {
+  return DType<DT>::to_float(raw_of_key<DT>(key));
+}
+
+// Probability mass of one element, relative to the row maximum m, in 2^-40
+// fixed point.  Integer sums are exact and order-independent, which keeps
+// the filter deterministic ([guide] §6.3: 默认确定性实现).
+__device__ __forceinline__ unsigned long long mass_fixed(float v, float m) {
+  const float e = expf(v - m);   // v <= m, so 0 <= e <= 1
+  return __float2ull_rn(e * kMassScaleF);
+}
+
+// round_D(1 - p): ``1 - p`` on a p tensor of the logits dtype
+// ([guide] §2 golden code and §3), clamped to [0, 1].
+template <int DT>
+__device__ __forceinline__ float top_p_threshold(const void* p, int64_t row) {
+  const float pv = DType<DT>::to_float(reinterpret_cast<const typename DType<DT>::raw*>(p)[row]);
+  float t = DType<DT>::round_to(1.0f - pv);
+  t = fmaxf(t, 0.0f);
+  return fminf(t, 1.0f);
+}
+
+// ------------------------------------------------------------------- PTX
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of an mbarrier, giving up after limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Full cluster barrier with release/acquire ordering of shared and global
+// memory (all threads of every CTA in the cluster must execute it).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ uint4 dsmem_ld_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long dsmem_ld_u64(uint32_t addr) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void dsmem_st_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+// ------------------------------------------------------------ block scans
+// Exclusive prefix sum over the CTA in thread order; *total gets the sum of
+// all threads.  `ws` is kWarps words of shared scratch.  Contains
+// __syncthreads(): every thread of the CTA must call it.
+__device__ __forceinline__ unsigned long long block_exclusive_scan(unsigned long long v,
+                                                                   unsigned long long* total,
+                                                                   unsigned long long* ws) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) ws[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long w = lane < kWarps ? ws[lane] : 0ull;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kWarps) ws[lane] = w;
+  }
+  __syncthreads();
+  const unsigned long long base = warp ? ws[warp - 1] : 0ull;
+  *total = ws[kWarps - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+__device__ __forceinline__ unsigned long long block_sum(unsigned long long v, unsigned long long* ws) {
+  unsigned long long t;
+  block_exclusive_scan(v, &t, ws);
+  return t;
+}
+
+}  // namespace topkp
