@@ -1,0 +1,307 @@
+"""Benchmark: fused top-k / top-p filtering of B=256 x V=128256 bf16 logits.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one topkp_apply call over the whole batch (joint top-k + top-p,
+workload 3: logits 2*N(0,1) in bf16, k ~ U{1..1024} with 10% of rows
+disabled, p ~ U[0.5,1] with 5% of rows at 1.0), inputs resident in HBM.
+Each timed step is bracketed by CUDA events on the launching stream, after a
+512 MiB memset that flushes L2 (the flush itself is outside the events).
+Under torchrun every rank filters its own batch (weak scaling, no collective:
+rows are independent); the reported time is the maximum over ranks.
+
+Prints one JSON line.  `roofline` compares the algorithmic bytes of the
+kernel (read logits + write out = 4 bytes per element) per launch with the
+measured HBM copy bandwidth; `cpu_baseline` times the CPU oracle (test
+infrastructure, single-threaded numpy) on a bounded sample of the same rows;
+`e2e` runs the same calls from pinned host buffers with the copies inside the
+timed region.  `--impl reference` times that oracle alone as the reference
+arm (on rank 0; other ranks exit without work).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+WORKLOAD = 3
+METRIC = "rows/s and achieved HBM GB/s (% of peak), B=256 V=128256 bf16 joint top-k+top-p"
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "top_logit_filter_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_per_launch():
+    """DRAM bytes per launch of the filter kernel from the committed ncu
+    summary, or None when the kernel sources changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "apply_kernel_B256_V128256_bf16.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_source_hash") != _kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _cpu_baseline(w, budget_s: float):
+    """The oracle as it stands, one row at a time, for about budget_s seconds."""
+    import oracle as O
+    t0 = time.perf_counter()
+    rows = 0
+    while rows < w["B"] and (rows < 4 or time.perf_counter() - t0 < budget_s):
+        O.apply_row(w["x"][rows], w["dtype"], w["p"][rows], int(w["k"][rows]))
+        rows += 1
+    dt = time.perf_counter() - t0
+    return {"value": rows / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {rows} rows of the B=256 x V=128256 bf16 workload, {dt:.1f} s, single-threaded numpy"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from top_logit_filter_gb300 import workloads
+    import oracle as O
+    w = workloads.make(WORKLOAD)
+    for i in range(args.warmup):
+        b = i % w["B"]
+        O.apply_row(w["x"][b], w["dtype"], w["p"][b], int(w["k"][b]))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        b = i % w["B"]
+        O.apply_row(w["x"][b], w["dtype"], w["p"][b], int(w["k"][b]))
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64+f32 (numpy)",
+        "data": "synthetic",
+        "config": {"workload": w["name"], "B": w["B"], "V": w["V"], "mode": "joint top-k + top-p",
+                   "step": "one row of the workload per step (CPU oracle)"},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} rows (cycling over the 256-row batch), single-threaded numpy"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import top_logit_filter_gb300 as tk
+    from rawutil import raw_to_torch
+    from top_logit_filter_gb300 import workloads
+
+    w = workloads.make(WORKLOAD)
+    B, V, dt = w["B"], w["V"], w["dtype"]
+    x = raw_to_torch(w["x"], dt, dev)
+    p = raw_to_torch(w["p"], dt, dev)
+    k = torch.from_numpy(w["k"]).to(dev)
+    out = torch.empty_like(x)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        tk.apply(x, p=p, k=k, out=out)
+    launches_per_step = tk.last_launch_count()
+    torch.cuda.synchronize(dev)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            tk.apply(x, p=p, k=k, out=out)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        if ws > 1:
+            torch.distributed.barrier()
+        t_wall = time.perf_counter() - t_wall
+    tk.device_status(dev)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_s = sum(step_ms) / 1e3
+    if ws > 1:
+        t = torch.tensor([total_s], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+    ms_per_step = 1e3 * total_s / args.steps
+    value = ws * B * args.steps / total_s
+
+    # roofline of the filter kernel: one launch per step
+    alg_bytes = B * V * 2 * 2
+    kernel_s = total_s / args.steps / max(1, launches_per_step)
+    achieved = alg_bytes / kernel_s / 1e9
+    peak, peak_kind = _peak_hbm()
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": _traffic_per_launch(), "peak_source": f"{peak_kind} (copy bandwidth, burst)",
+                "algorithmic_bytes_per_launch": alg_bytes}
+
+    # end to end through the public API from pinned host buffers
+    hx = raw_to_torch(w["x"], dt).pin_memory()
+    hp = raw_to_torch(w["p"], dt).pin_memory()
+    hk = torch.from_numpy(w["k"]).pin_memory()
+    hout = torch.empty_like(hx).pin_memory()
+    e2e_steps = max(3, min(50, args.steps))
+    dx, dp, dk = torch.empty_like(x), torch.empty_like(p), torch.empty_like(k)
+    for _ in range(2):
+        dx.copy_(hx, non_blocking=True); dp.copy_(hp, non_blocking=True); dk.copy_(hk, non_blocking=True)
+        hout.copy_(tk.apply(dx, p=dp, k=dk), non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        dx.copy_(hx, non_blocking=True); dp.copy_(hp, non_blocking=True); dk.copy_(hk, non_blocking=True)
+        hout.copy_(tk.apply(dx, p=dp, k=dk), non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    h2d = hx.numel() * hx.element_size() + hp.numel() * hp.element_size() + hk.numel() * hk.element_size()
+    d2h = hout.numel() * hout.element_size()
+    e2e = {"value": ws * B * e2e_steps / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": e2e_steps}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w["name"], "B": B, "V": V, "mode": "joint top-k + top-p",
+                       "l2": "flushed before every timed step (512 MiB memset, outside the events)",
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU",
+                       "wall_s_timed_region": t_wall},
+            "achieved_GBps": achieved,
+            "roofline": roofline,
+            "gpu_launches": args.steps * launches_per_step,
+            "clocks": clocks.summary(),
+            "e2e": e2e,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = _cpu_baseline(w, args.cpu_budget)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing (profiling runs)")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

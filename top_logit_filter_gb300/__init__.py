@@ -45,8 +45,16 @@ def _check(status: int):
         raise TopKPError(status, _lib.last_error())
 
 
+# Address passed for a tensor that is present but empty (its data pointer can
+# be NULL, which the C ABI reads as "absent"); empty problems return before
+# any pointer is dereferenced.
+_EMPTY = 16
+
+
 def _ptr(t):
-    return None if t is None else t.data_ptr()
+    if t is None:
+        return None
+    return t.data_ptr() or (_EMPTY if t.numel() == 0 else None)
 
 
 def _stream(device):
