@@ -64,7 +64,8 @@ def _check_all(out, x, dtype, p, k, where):
     return flips
 
 
-PLANS = ["", "1,1", "2,1", "3,1", "4,0", "5,1", "8,1", "2,0"]
+# TOPKP_FORCE_PLAN: bytes per ring slot ("" = the planner's choice).
+PLANS = ["", "8192", "32768"]
 
 
 @pytest.mark.parametrize("dtype", DTS)
@@ -84,15 +85,15 @@ def test_small_rows_all_plans(tk, monkeypatch, dtype, V, mode):
 
 @pytest.mark.parametrize("dtype", DTS)
 def test_multi_slice_rows(tk, monkeypatch, dtype):
-    """Rows long enough that every CTA of a cluster holds several vectors and
-    a ragged last slice."""
+    """Rows long enough to cycle the shared-memory ring several times, with a
+    partial last chunk and a tail shorter than 16 bytes."""
     rng = np.random.default_rng(3)
     B, V = 6, 40011
     for kind in ("normal", "ties"):
         x = _rows(rng, B, V, dtype, kind)
         k, p = _kp(rng, B, V, dtype, "kp")
         k[:3] = [0, 37, 900]
-        for plan in ("", "1,1", "4,1", "7,1", "16,1", "8,0"):
+        for plan in ("", "8192", "32768"):
             monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
             out = _run_apply(tk, x, dtype, p, k)
             _check_all(out, x, dtype, p, k, f"{dtype} {kind} plan={plan!r}")
@@ -180,3 +181,23 @@ def test_workload_full_size(tk, wl, sample):
             kth = np.partition(xv[b], w["V"] - kk)[w["V"] - kk]
             exp = np.where(xv[b] >= kth, bits(w["x"][b], dt), NEG_INF[dt])
             assert np.array_equal(ob[b], exp), f"row {b}"
+
+
+@pytest.mark.parametrize("mode", ["topp_only", "topk_only", "all_rows_joint"])
+def test_workload3_mode_variants_full_size(tk, mode):
+    """The B=256 x V=128256 bf16 rows with one filter dropped (or every row
+    joint), so each launch runs one kernel path on every row."""
+    from top_logit_filter_gb300 import workloads
+    w = workloads.make(3)
+    dt = "bf16"
+    k = None if mode == "topp_only" else np.where(w["k"] > 0, w["k"], 512).astype(np.int32)
+    p = None if mode == "topk_only" else w["p"]
+    xt = raw_to_torch(w["x"], dt, "cuda")
+    out = torch_to_raw(tk.apply(xt, p=None if p is None else raw_to_torch(p, dt, "cuda"),
+                                k=None if k is None else torch.from_numpy(k).cuda()), dt)
+    tk.device_status()
+    flips = 0
+    for b in np.random.default_rng(7).choice(w["B"], 40, replace=False):
+        _, info = O.apply_row(w["x"][b], dt, None if p is None else p[b], None if k is None else int(k[b]))
+        flips += compare_row(out[b], w["x"][b], info, dt, where=f"{mode} row {b}")
+    print(f"{mode}: {flips} top-p flips inside the band")

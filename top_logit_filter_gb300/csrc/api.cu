@@ -64,6 +64,19 @@ int current_sms(int* dev_out) {
   return sms;
 }
 
+// L2 size of a device (cached per device).
+int64_t current_l2_bytes(int dev) {
+  static int64_t cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
+    cudaGetLastError();
+    v = 64 << 20;
+  }
+  if (dev >= 0 && dev < 64) cache[dev] = v;
+  return v;
+}
+
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s for any single bounded wait
 
 }  // namespace
@@ -74,48 +87,20 @@ static int slice_for(int64_t V, int C) {
   return (int)((s + 15) / 16 * 16);
 }
 
-ApplyPlan plan_apply(int64_t B, int64_t V, int esize, int num_sms, const char* force) {
+ApplyPlan plan_apply(int64_t B, int64_t V, int esize, int num_sms, int64_t l2_bytes, const char* force) {
   ApplyPlan p;
+  // Two CTAs per SM keep a decode batch of up to 2 x SMs rows in one wave.
+  // The rows of a wave must stay in L2 between the HBM pass and the later
+  // passes; longer rows get one CTA per SM (and larger slots).
+  const int64_t row_bytes = V * esize;
+  const int64_t resident2 = B < 2LL * num_sms ? B : 2LL * num_sms;
+  p.ctas_per_sm = (resident2 * row_bytes > l2_bytes * 3 / 4) ? 1 : 2;
+  p.chunk = p.ctas_per_sm == 2 ? 16384 : 32768;
   if (force && *force) {
-    int c = 1, st = 1;
-    if (sscanf(force, "%d,%d", &c, &st) >= 1) {
-      c = c < 1 ? 1 : (c > 16 ? 16 : c);
-      while (c > 1 && (int64_t)(c - 1) * slice_for(V, c) >= V) --c;
-      p.csize = c;
-      p.slice = slice_for(V, c);
-      p.staged = st != 0;
-      p.smem = apply_smem_bytes(p.slice, esize, p.staged);
-      if (p.smem <= 227 * 1024) return p;
-    }
+    int c = 0;
+    if (sscanf(force, "%d", &c) == 1 && c >= 8192) p.chunk = (c > 32768 ? 32768 : c) / 8192 * 8192;
   }
-  // Prefer two CTAs per SM (<= 110 KB each), then one per SM, up to 16 CTAs
-  // per row; beyond that, re-read the row from global memory (L2).
-  const size_t budgets[2] = {110 * 1024, 227 * 1024};
-  const int cmax[2] = {8, 16};
-  for (int pass = 0; pass < 2; ++pass) {
-    for (int c = 1; c <= cmax[pass]; ++c) {
-      const int s = slice_for(V, c);
-      if (c > 1 && (int64_t)(c - 1) * s >= V) break;
-      if (apply_smem_bytes(s, esize, true) <= budgets[pass]) {
-        p.csize = c;
-        p.slice = s;
-        p.staged = true;
-        // few rows: spread each row over more SMs
-        while (p.csize < 8 && B * p.csize < 2LL * num_sms) {
-          const int s2 = slice_for(V, p.csize + 1);
-          if (s2 < 2048 || (int64_t)p.csize * s2 >= V) break;
-          ++p.csize;
-          p.slice = s2;
-        }
-        p.smem = apply_smem_bytes(p.slice, esize, true);
-        return p;
-      }
-    }
-  }
-  p.csize = 8;
-  p.slice = slice_for(V, 8);
-  p.staged = false;
-  p.smem = apply_smem_bytes(p.slice, esize, false);
+  p.smem = apply_smem_bytes(p.chunk);
   return p;
 }
 
@@ -176,7 +161,7 @@ topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_lo
   int dev = 0;
   const int sms = current_sms(&dev);
   if (sms <= 0) return fail(TOPKP_ERR_LAUNCH, "topkp_apply: no usable CUDA device");
-  const ApplyPlan plan = plan_apply(B, V, es, sms, getenv("TOPKP_FORCE_PLAN"));
+  const ApplyPlan plan = plan_apply(B, V, es, sms, current_l2_bytes(dev), getenv("TOPKP_FORCE_PLAN"));
 
   ApplyArgs a = {};
   a.x = logits;
@@ -186,13 +171,12 @@ topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_lo
   a.ldx = ld_logits;
   a.ldo = ld_out;
   a.V = (int32_t)V;
-  a.slice = plan.slice;
-  a.csize = plan.csize;
-  a.bulk_in = ((uintptr_t)logits % 16 == 0) && ((ld_logits * es) % 16 == 0);
+  a.chunk = plan.chunk;
+  a.aligned = ((uintptr_t)logits % 16 == 0) && ((ld_logits * es) % 16 == 0);
   a.vec_out = ((uintptr_t)out % 16 == 0) && ((ld_out * es) % 16 == 0);
   a.timeout_ns = kTimeoutNs;
-  // grid.x = rows * csize must stay below 2^31
-  const int64_t max_rows = (INT_MAX / plan.csize);
+  // one CTA per row; grid.x must stay below 2^31
+  const int64_t max_rows = INT_MAX;
   int launches = 0;
   for (int64_t r0 = 0; r0 < B; r0 += max_rows) {
     const int64_t nb = B - r0 < max_rows ? B - r0 : max_rows;
@@ -205,8 +189,8 @@ topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_lo
     const cudaError_t e = launch_apply(dtype, plan, ai, (cudaStream_t)stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
-      return fail(TOPKP_ERR_LAUNCH, "topkp_apply: launch failed (%s; csize=%d slice=%d smem=%zu)", cudaGetErrorString(e),
-                  plan.csize, plan.slice, plan.smem);
+      return fail(TOPKP_ERR_LAUNCH, "topkp_apply: launch failed (%s; chunk=%d smem=%zu)", cudaGetErrorString(e),
+                  plan.chunk, plan.smem);
     }
     ++launches;
   }

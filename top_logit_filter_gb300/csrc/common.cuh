@@ -11,7 +11,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
-#include "../../include/topkp.h"
+#include "topkp.h"
 
 namespace topkp {
 
@@ -74,11 +74,24 @@ __device__ __forceinline__ float value_of_key(uint32_t key) {
 }
 
 // Probability mass of one element, relative to the row maximum m, in 2^-40
-// fixed point.  Integer sums are exact and order-independent, which keeps
-// the filter deterministic ([guide] §6.3: 默认确定性实现).
-__device__ __forceinline__ unsigned long long mass_fixed(float v, float m) {
-  const float e = expf(v - m);   // v <= m, so 0 <= e <= 1
-  return __float2ull_rn(e * kMassScaleF);
+// fixed point: exp(v - m) = 2^((v - m) log2 e), evaluated as one fused
+// multiply-add and the hardware base-2 exponential (relative error about
+// 2e-6 for |v - m| <= 40, far inside the 1e-5 tolerance on the cumulative
+// probability).  Integer sums are exact and order-independent, which keeps
+// the filter deterministic ([guide] §6.3: 默认确定性实现).  The function is
+// the only source of masses, so equal values always get equal masses.
+struct MassRef {
+  float neg_m_log2e;
+  __device__ explicit MassRef(float m) : neg_m_log2e(-m * 1.4426950408889634f) {}
+};
+__device__ __forceinline__ float mass_f32(float v, const MassRef& r) {
+  const float t = fminf(fmaf(v, 1.4426950408889634f, r.neg_m_log2e), 0.0f);
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(t));
+  return e;
+}
+__device__ __forceinline__ unsigned long long mass_fixed(float v, const MassRef& r) {
+  return __float2ull_rn(mass_f32(v, r) * kMassScaleF);
 }
 
 // round_D(1 - p): ``1 - p`` on a p tensor of the logits dtype
@@ -119,6 +132,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -151,6 +168,42 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// L2 eviction policies and 16-byte global accesses that carry them.  Rows
+// that the write pass reads again are loaded with evict_last; the final
+// read and the output stores use evict_first.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_global_hint(const void* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st_global_hint(void* ptr, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(pol)
+               : "memory");
+}
+
+// 1-D bulk copy global -> shared with an L2 eviction policy.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -161,6 +214,15 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 // memory (all threads of every CTA in the cluster must execute it).
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The two halves of a cluster barrier, for a CTA that must stay resident
+// until its peers have finished reading its shared memory.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
@@ -188,6 +250,10 @@ __device__ __forceinline__ unsigned long long dsmem_ld_u64(uint32_t addr) {
   unsigned long long v;
   asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
   return v;
+}
+
+__device__ __forceinline__ void dsmem_st_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
 __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {

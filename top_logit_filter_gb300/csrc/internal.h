@@ -4,14 +4,15 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/topkp.h"
+#include "topkp.h"
 
 namespace topkp {
 
 // ---------------------------------------------------------------- apply
-// One row of logits is split into `csize` contiguous slices of `slice`
-// elements; the CTAs of one thread-block cluster take one slice each and
-// cooperate through distributed shared memory.
+// One CTA filters one row.  The row streams through a ring of kApplySlots
+// chunk-sized slots in shared memory, filled by single large bulk copies:
+// once from HBM, then again from L2 for the later passes.  Warp w handles
+// the w-th sixteenth of every chunk.
 struct ApplyArgs {
   const void* x;          // logits [B, ldx]
   void* out;              // out [B, ldo]
@@ -20,33 +21,35 @@ struct ApplyArgs {
   int64_t ldx, ldo;       // row strides, elements
   int64_t B;
   int32_t V;
-  int32_t slice;          // elements per CTA (multiple of 16)
-  int32_t csize;          // CTAs per row (= cluster size)
-  int32_t bulk_in;        // rows of x are 16-byte aligned: bulk copies / vector loads
+  int32_t chunk;          // bytes per ring slot (multiple of 8 KB)
+  int32_t aligned;        // rows of x are 16-byte aligned: bulk copies / vector loads
   int32_t vec_out;        // rows of out are 16-byte aligned: vector stores
-  int32_t pad_;
   uint64_t timeout_ns;    // limit of every bounded wait
 };
 
 struct ApplyPlan {
-  int csize = 1;
-  int slice = 0;
-  bool staged = true;
+  int chunk = 16384;
+  int ctas_per_sm = 2;
   size_t smem = 0;        // dynamic shared memory per CTA
 };
 
-constexpr int kApplyChunks = 4;       // bulk copies (and mbarriers) per slice
-constexpr size_t kApplyHdrBytes = 512;
-constexpr size_t kApplyFixedSmem = kApplyHdrBytes + 2048 * 4 + 2048 * 8;
+// Shared memory of one apply CTA: header (mbarriers, small histograms), a
+// 4096-bin histogram, a 24 KB region for the per-warp candidate lists (or
+// per-warp window counts, or generic-path mass bins), then the ring.
+constexpr int kApplyWarps = 16;
+constexpr int kApplySlots = 4;
+constexpr size_t kApplyHdrBytes = 4096;
+constexpr size_t kApplyHistBytes = 4096 * 4;
+constexpr size_t kApplyBigBytes = 24576;
+constexpr size_t kApplyFixedSmem = kApplyHdrBytes + kApplyHistBytes + kApplyBigBytes;
 
-inline size_t apply_smem_bytes(int slice, int esize, bool staged) {
-  return kApplyFixedSmem + (staged ? ((size_t)slice * esize + 127) / 128 * 128 : 0);
-}
+inline size_t apply_smem_bytes(int chunk) { return kApplyFixedSmem + (size_t)kApplySlots * chunk; }
 
 cudaError_t launch_apply(topkp_dtype dt, const ApplyPlan& plan, const ApplyArgs& a, cudaStream_t s);
 
-// Chooses csize / slice / staging for a problem; `num_sms` of the device.
-ApplyPlan plan_apply(int64_t B, int64_t V, int esize, int num_sms, const char* force);
+// Chooses the ring slot size and CTAs per SM for a problem on a device with
+// `num_sms` SMs and `l2_bytes` of L2.
+ApplyPlan plan_apply(int64_t B, int64_t V, int esize, int num_sms, int64_t l2_bytes, const char* force);
 
 // --------------------------------------------------------------- sorted
 struct SortedArgs {

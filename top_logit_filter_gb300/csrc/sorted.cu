@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 2) sorted_kernel(const SortedArgs a)
   // ---- top-p boundary ([guide] §2 steps 4-7) ----
   int J = jk;
   if (topp) {
-    const float m = D::to_float(sv[V - 1]);
+    const MassRef m(D::to_float(sv[V - 1]));
     const float thr = top_p_threshold<DT>(a.p, row);
     const int tail = V - jk;
     const int per_cta = (tail + C - 1) / C;
