@@ -64,19 +64,6 @@ int current_sms(int* dev_out) {
   return sms;
 }
 
-// L2 size of a device (cached per device).
-int64_t current_l2_bytes(int dev) {
-  static int64_t cache[64] = {0};
-  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
-  int v = 0;
-  if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
-    cudaGetLastError();
-    v = 64 << 20;
-  }
-  if (dev >= 0 && dev < 64) cache[dev] = v;
-  return v;
-}
-
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s for any single bounded wait
 
 }  // namespace
@@ -85,23 +72,6 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s for any single bounded wa
 static int slice_for(int64_t V, int C) {
   const int64_t s = (V + C - 1) / C;
   return (int)((s + 15) / 16 * 16);
-}
-
-ApplyPlan plan_apply(int64_t B, int64_t V, int esize, int num_sms, int64_t l2_bytes, const char* force) {
-  ApplyPlan p;
-  // Two CTAs per SM keep a decode batch of up to 2 x SMs rows in one wave.
-  // The rows of a wave must stay in L2 between the HBM pass and the later
-  // passes; longer rows get one CTA per SM (and larger slots).
-  const int64_t row_bytes = V * esize;
-  const int64_t resident2 = B < 2LL * num_sms ? B : 2LL * num_sms;
-  p.ctas_per_sm = (resident2 * row_bytes > l2_bytes * 3 / 4) ? 1 : 2;
-  p.chunk = p.ctas_per_sm == 2 ? 16384 : 32768;
-  if (force && *force) {
-    int c = 0;
-    if (sscanf(force, "%d", &c) == 1 && c >= 8192) p.chunk = (c > 32768 ? 32768 : c) / 8192 * 8192;
-  }
-  p.smem = apply_smem_bytes(p.chunk);
-  return p;
 }
 
 SortedPlan plan_sorted(int64_t B, int64_t V, int esize, int num_sms, bool with_logits, const char* force) {
@@ -150,6 +120,8 @@ topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_lo
   if (ld_logits < V || ld_out < V)
     return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: row stride below V (ld_logits=%lld ld_out=%lld V=%lld)",
                 (long long)ld_logits, (long long)ld_out, (long long)V);
+  if ((uintptr_t)logits % es || (uintptr_t)out % es || (p && (uintptr_t)p % es) || (k && (uintptr_t)k % 4))
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: a pointer is not aligned to its element size");
   const size_t xbytes = (size_t)((B - 1) * ld_logits + V) * es;
   const size_t obytes = (size_t)((B - 1) * ld_out + V) * es;
   const bool in_place = (logits == out && ld_logits == ld_out);
@@ -161,7 +133,7 @@ topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_lo
   int dev = 0;
   const int sms = current_sms(&dev);
   if (sms <= 0) return fail(TOPKP_ERR_LAUNCH, "topkp_apply: no usable CUDA device");
-  const ApplyPlan plan = plan_apply(B, V, es, sms, current_l2_bytes(dev), getenv("TOPKP_FORCE_PLAN"));
+  const char* force = getenv("TOPKP_FORCE_PLAN");
 
   ApplyArgs a = {};
   a.x = logits;
@@ -171,10 +143,7 @@ topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_lo
   a.ldx = ld_logits;
   a.ldo = ld_out;
   a.V = (int32_t)V;
-  a.chunk = plan.chunk;
-  a.aligned = ((uintptr_t)logits % 16 == 0) && ((ld_logits * es) % 16 == 0);
-  a.vec_out = ((uintptr_t)out % 16 == 0) && ((ld_out * es) % 16 == 0);
-  a.timeout_ns = kTimeoutNs;
+  a.force = (force && strcmp(force, "generic") == 0) ? kApplyForceGeneric : 0;
   // one CTA per row; grid.x must stay below 2^31
   const int64_t max_rows = INT_MAX;
   int launches = 0;
@@ -186,11 +155,10 @@ topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_lo
     ai.out = (char*)out + r0 * ld_out * es;
     ai.p = p ? (const char*)p + r0 * es : nullptr;
     ai.k = k ? k + r0 : nullptr;
-    const cudaError_t e = launch_apply(dtype, plan, ai, (cudaStream_t)stream);
+    const cudaError_t e = launch_apply(dtype, ai, (cudaStream_t)stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
-      return fail(TOPKP_ERR_LAUNCH, "topkp_apply: launch failed (%s; chunk=%d smem=%zu)", cudaGetErrorString(e),
-                  plan.chunk, plan.smem);
+      return fail(TOPKP_ERR_LAUNCH, "topkp_apply: launch failed (%s; smem=%zu)", cudaGetErrorString(e), kApplySmem);
     }
     ++launches;
   }
@@ -269,14 +237,13 @@ topkp_status topkp_device_status(void* stream) {
     cudaGetLastError();
     return fail(TOPKP_ERR_LAUNCH, "topkp_device_status: stream error: %s", cudaGetErrorString(e));
   }
-  unsigned int w1 = 0, w2 = 0;
-  e = apply_take_device_error(&w1);
-  if (e == cudaSuccess) e = sorted_take_device_error(&w2);
+  unsigned int w = 0;
+  e = sorted_take_device_error(&w);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return fail(TOPKP_ERR_LAUNCH, "topkp_device_status: cannot read the device error word: %s", cudaGetErrorString(e));
   }
-  if (w1 | w2) return fail(TOPKP_ERR_DEVICE_TIMEOUT, "topkp_device_status: a kernel gave up a bounded wait");
+  if (w) return fail(TOPKP_ERR_DEVICE_TIMEOUT, "topkp_device_status: a kernel gave up a bounded wait");
   return TOPKP_SUCCESS;
 }
 

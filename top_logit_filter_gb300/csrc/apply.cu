@@ -10,40 +10,43 @@
 //
 // Launch shape: one 512-thread CTA per row, two CTAs per SM, so a decode
 // batch of a few hundred rows runs as a single wave and every row's latency
-// overlaps every other row's.  The row streams through a ring of four large
-// shared-memory slots, each filled by one bulk copy (TMA, cp.async.bulk; few
-// large copies keep the per-copy cost negligible), and warp w handles the
-// w-th sixteenth of every slot.  The first pass reads HBM; the later passes
-// read the same bytes again from L2, so HBM sees each logit read once and
-// each output written once.
+// overlaps every other row's.  Warp w owns the w-th sixteenth of the row's
+// 16-byte vectors (warp 0 also the unaligned head, the last warp the tail);
+// its lanes read consecutive vectors straight into registers, several loads
+// in flight per lane, so every warp load is one coalesced 512-byte access.
+// The first pass reads HBM; later passes read the same bytes again from L2
+// (the final one with an evict-first hint), so HBM sees each logit read once
+// and each output written once.
 //
 // Rows with top-k take the candidate path:
-//   1. one packed max per 16-byte vector and a histogram of those vector
-//      maxima over a 12-bit first digit;
+//   1. pass A: one packed max per 16-byte vector, the row max, and a
+//      histogram of the vector maxima over a 12-bit first digit;
 //   2. the k-th largest vector maximum lower-bounds the row's k-th largest
 //      element (k distinct elements reach it); its bucket floor L decides
-//      candidacy.  A second pass tests every vector with one packed ">= L"
-//      compare and each warp appends the few elements >= L to its own list;
+//      candidacy.  Pass B tests every vector with one packed ">= L" compare
+//      and each warp appends the few elements >= L to its own list;
 //   3. the selection runs on the lists alone: the k-th largest key by counts,
 //      then the top-p cut by probability mass (2^-40 fixed point; for 16-bit
 //      dtypes an exact per-key histogram, so mass = count x exp(value - max)).
-
 // Rows with top-p only (fp16 / bf16) take the window path:
-//   1. phase 1 counts every element per first-digit bucket;
+//   1. pass A counts every element per first-digit bucket;
 //   2. rigorous lower / upper bounds of every bucket's mass (count times the
 //      mass of its smallest / largest value) bracket the top-p cut into a
 //      window of buckets;
-//   3. one pass computes every element's mass: the row total and the mass
+//   3. pass B computes every element's mass: the row total and the mass
 //      below the window accumulate in registers (fp32 per 16-byte vector,
-//      then 2^-40 fixed point), the window gets exact per-key counts; the
-//      cut follows from count x mass per key.
+//      then 2^-40 fixed point), the window gets exact per-key counts per
+//      warp; the cut follows from count x mass per key.
 // Everything else (fp32 top-p-only rows, candidate overflow, wide windows)
 // takes the generic path: a radix descent over the whole row (11-bit first
 // digit, then 5 bits for 16-bit keys or 11 + 10 for fp32).
 //
-// When the cut falls inside a run of equal values, the write pass ranks the
-// ties in index order on the fly: per slot, a scan over the warps' tie
-// counts, then a warp scan within each sixteenth.
+// When the cut falls inside a run of equal values, the write pass needs each
+// tie's rank in index order.  The ties of T in each warp's sixteenth are
+// known before the write pass (from the warp's candidate list, its window
+// histogram, or a counting pass), so a warp whose ties are all masked or all
+// kept applies one compare; the single warp where the cut falls ranks its
+// ties with warp scans.
 #include <type_traits>
 
 #include "common.cuh"
@@ -51,25 +54,21 @@
 
 namespace topkp {
 
-static __device__ unsigned int g_device_error = 0;
-
 constexpr int kBins = 4096;                  // candidate / window path first digit: 12 bits
 constexpr int kSmallBins = 256;              // 8-bit digits over candidate lists
-constexpr int kWinKeys = (int)(kApplyBigBytes / 4 / kApplyWarps);  // window keys per warp histogram
-static_assert(kApplyWarps == kWarps, "one region per warp");
+constexpr int kWinKeys = (int)(kApplyBigBytes / 4 / kWarps);  // window keys per warp histogram
+constexpr int kLoadsSimple = 8;              // vectors in flight per lane, light per-vector work
+constexpr int kLoadsHeavy = 4;               // vectors in flight per lane, per-element work
 
 struct __align__(16) ApplyHdr {
-  uint64_t full[kApplySlots];           // ring slot filled (bulk copy landed)
-  uint64_t empty[kApplySlots];          // ring slot drained (one arrival per warp)
   unsigned long long ws[kWarps];        // block-scan scratch
   unsigned long long sel_off;           // select result: count/mass outside the bin
   unsigned long long small_mass[kSmallBins];
   uint32_t small_cnt[kSmallBins];
-  uint32_t nseg[kApplyWarps];           // candidates in each warp's list
-  uint32_t wtie[2][kApplyWarps];        // write pass: ties of T per warp sub-block, by chunk parity
+  uint32_t nseg[kWarps];                // candidates in each warp's list
+  uint32_t wtie[kWarps];                // ties of T in each warp's sixteenth of the row
   int sel_bin;                          // select result: bin, -1 if none
   uint32_t maxkey;                      // row max key
-  uint32_t failed;                      // a bounded wait gave up
   uint32_t over;                        // a candidate list overflowed
 };
 static_assert(sizeof(ApplyHdr) <= kApplyHdrBytes, "header too large");
@@ -264,10 +263,14 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
   return v;
 }
 
+
 enum TieRule : int { kTiesKept = 0, kTiesMasked = 1, kTiesStraddle = 2, kKeepAll = 3 };
 
 template <int DT>
 using CandKey = typename std::conditional<DType<DT>::kKeyBits == 16, uint16_t, uint32_t>::type;
+
+template <int N>
+using Loads = std::integral_constant<int, N>;
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
@@ -280,13 +283,12 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   constexpr int KB = D::kKeyBits;
   constexpr int SHB = KB - 12;           // 12-bit first digit of the candidate / window paths
   constexpr int SH1 = L::shift(0);       // 11-bit first digit of the generic path
-  constexpr int CAPW = (int)(kApplyBigBytes / sizeof(ckey)) / kApplyWarps;  // list entries per warp
+  constexpr int CAPW = (int)(kApplyBigBytes / sizeof(ckey)) / kWarps;  // list entries per warp
 
   extern __shared__ __align__(128) unsigned char smem[];
   ApplyHdr& h = *reinterpret_cast<ApplyHdr*>(smem);
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kApplyHdrBytes);
   unsigned char* big = smem + kApplyHdrBytes + kApplyHistBytes;
-  unsigned char* ring = smem + kApplyFixedSmem;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -298,131 +300,97 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   uint32_t* whist = reinterpret_cast<uint32_t*>(big) + warp * kWinKeys;
   unsigned long long* mass = reinterpret_cast<unsigned long long*>(big);
 
+  const bool generic_only = (a.force & kApplyForceGeneric) != 0;
   const int kv = a.k ? a.k[row] : 0;
   const bool topk = a.k != nullptr && kv >= 1 && kv <= V - 1;
   const bool topp = a.p != nullptr;
   const bool keepall = !topk && !topp;
-  const bool window = !topk && topp && KB == 16;
+  const bool window = !topk && topp && KB == 16 && !generic_only;
+  const bool in_place = reinterpret_cast<const void*>(xr) == reinterpret_cast<const void*>(orow);
+  if (keepall && in_place) return;  // nothing to filter, nothing to move
 
-  const uint64_t pol_last = l2_policy_evict_first();
-
-  // ---- ring geometry ----
-  const int CH = a.chunk;                         // bytes per slot
-  const int CHE = CH / (int)sizeof(raw);          // elements per slot
-  const int SUBV = CH / 16 / kApplyWarps;         // vectors per warp per slot
-  const int nbytes = V * (int)sizeof(raw);
-  const bool aligned = a.aligned != 0;
-  const int nb16 = aligned ? (nbytes & ~15) : 0;  // bytes moved by bulk copies
-  const int body = aligned ? nb16 / (int)sizeof(raw) : V;  // elements in whole chunks
-  const int nch = (body * (int)sizeof(raw) + CH - 1) / CH;
-  const bool has_tail = body < V;                 // aligned rows: the last < 16 bytes
+  // ---- row geometry: unaligned head, whole 16-byte vectors, tail ----
+  const uintptr_t xaddr = reinterpret_cast<uintptr_t>(xr);
+  const int head = min(V, (int)(((16u - (uint32_t)(xaddr & 15u)) & 15u) / (uint32_t)sizeof(raw)));
+  const int nvec = (V - head) / VEC;
+  const int tail = V - head - nvec * VEC;
+  const uint4* xv = reinterpret_cast<const uint4*>(xr + head);
+  const int per_warp = (nvec + kWarps - 1) / kWarps;
+  const int wb = min(nvec, warp * per_warp);
+  const int we = min(nvec, wb + per_warp);
+  const int nsteps = (we - wb + 31) / 32;  // warp-uniform
+  const bool vec_out = ((reinterpret_cast<uintptr_t>(orow) ^ xaddr) & 15u) == 0;
+  const uint32_t NEG2 = P::splat((uint32_t)D::kNegInf);
+  const uint64_t pol_first = l2_policy_evict_first();
 
   if (tid == 0) {
     h.maxkey = 0;
-    h.failed = 0;
     h.over = 0;
     h.sel_bin = -1;
-    for (int i = 0; i < kApplySlots; ++i) {
-      mbar_init(&h.full[i], 1);
-      mbar_init(&h.empty[i], kApplyWarps);
-    }
-    fence_mbar_init();
   }
-  if (topk || window)
+  if ((topk && !generic_only) || window)
     for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
   __syncthreads();
 
-  uint32_t used = 0;  // chunks consumed so far, all passes (CTA-uniform)
-  bool my_fail = false;
-  // thread 0: start the bulk copy of chunk c of the current pass (global chunk used + c)
-  auto issue = [&](int c, bool last_use) {
-    const uint32_t g = used + (uint32_t)c;
-    const int slot = (int)(g % kApplySlots);
-    if (g >= (uint32_t)kApplySlots &&
-        !mbar_wait_bounded(&h.empty[slot], ((g / kApplySlots) - 1u) & 1u, a.timeout_ns))
-      my_fail = true;
-    const uint32_t bytes = (uint32_t)min(CH, nb16 - c * CH);
-    mbar_arrive_expect_tx(&h.full[slot], bytes);
-    const unsigned char* src = reinterpret_cast<const unsigned char*>(xr) + (size_t)c * CH;
-    if (last_use) bulk_g2s_hint(ring + slot * CH, src, bytes, &h.full[slot], pol_last);
-    else bulk_g2s(ring + slot * CH, src, bytes, &h.full[slot]);
-  };
-  // This warp's vectors of chunk c, in index order: f(e, q, nv) with q the
-  // 16 bytes at row offsets e .. e+VEC-1, nv of them valid (0 on idle lanes).
-  // The invalid elements of a partial vector hold -inf, which never exceeds
-  // a valid element and has zero mass.  slot < 0: the tail after the last
-  // whole chunk.  All lanes call f together.
-  const uint32_t NEG2 = P::splat((uint32_t)D::kNegInf);
-  auto warp_chunk = [&](int c, int slot, auto&& f) {
-    if (slot < 0) {
-      if (warp == 0) {
-        uint4 q = make_uint4(NEG2, NEG2, NEG2, NEG2);
-        raw* r = reinterpret_cast<raw*>(&q);
-        int nv = 0;
-        if (lane == 0) {
-          nv = V - body;
+  // n elements from row offset e0 as a vector, the rest -inf
+  auto load_partial = [&](int e0, int n) -> uint4 {
+    uint32_t w[4] = {NEG2, NEG2, NEG2, NEG2};
 #pragma unroll
-          for (int j = 0; j < VEC; ++j)
-            if (j < nv) r[j] = xr[body + j];
-        }
-        f(body, q, nv);
-      }
-      return;
-    }
-    const int valid = min(CHE, body - c * CHE);
-    for (int s = 0; s < SUBV; s += 32) {
-      const int v = warp * SUBV + s + lane;
-      const int e = c * CHE + v * VEC;
-      const int nv = max(0, min(VEC, valid - v * VEC));
-      uint4 q = make_uint4(NEG2, NEG2, NEG2, NEG2);
-      if (nv > 0) {
-        if (aligned) {
-          q = *reinterpret_cast<const uint4*>(ring + slot * CH + v * 16);
+    for (int j = 0; j < VEC; ++j) {
+      if (j < n) {
+        const uint32_t b = (uint32_t)xr[e0 + j];
+        if (KB == 16) {
+          const int sh = (j & 1) * 16;
+          w[j >> 1] = (w[j >> 1] & ~(0xffffu << sh)) | (b << sh);
         } else {
-          raw* r = reinterpret_cast<raw*>(&q);
-#pragma unroll
-          for (int j = 0; j < VEC; ++j)
-            if (j < nv) r[j] = xr[e + j];
+          w[j] = b;
         }
       }
-      f(e, q, nv);
     }
+    return make_uint4(w[0], w[1], w[2], w[3]);
   };
-  // One pass over the row: per_chunk(c, slot) runs on every thread for every
-  // chunk (slot -1: the tail), in order.  last_use: the final read of the row.
-  auto stream = [&](bool last_use, auto&& per_chunk) {
-    if (aligned && tid == 0) {
-      fence_proxy_async_shared();  // earlier reads of the slots precede the new copies
-      for (int c = 0; c < min(nch, kApplySlots); ++c) issue(c, last_use);
+  // One pass over the row: f(e, q, nv) for this warp's vectors in index
+  // order, q = the 16 bytes at row offsets e .. e+VEC-1 with nv of them valid
+  // (-inf in the others, which never exceeds a valid element and has zero
+  // mass; nv = 0 on idle lanes).  All lanes of a warp call f together.  U
+  // vectors per lane are in flight; last: the final read of the row.
+  auto sweep = [&](auto U_c, bool last, auto&& f) {
+    constexpr int U = decltype(U_c)::value;
+    if (warp == 0 && head > 0) {
+      const uint4 q = load_partial(0, lane == 0 ? head : 0);
+      f(0, q, lane == 0 ? head : 0);
     }
-    for (int c = 0; c < nch; ++c) {
-      const uint32_t g = used + (uint32_t)c;
-      const int slot = (int)(g % kApplySlots);
-      if (aligned && !mbar_wait_bounded(&h.full[slot], (g / kApplySlots) & 1u, a.timeout_ns)) my_fail = true;
-      per_chunk(c, slot);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&h.empty[slot]);
-      if (aligned && tid == 0 && c + kApplySlots < nch) {
-        fence_proxy_async_shared();
-        issue(c + kApplySlots, last_use);
+    for (int s0 = 0; s0 < nsteps; s0 += U) {
+      uint4 q[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = wb + (s0 + u) * 32 + lane;
+        q[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
+        if (v < we) q[u] = last ? ld_global_hint(xv + v, pol_first) : __ldcg(xv + v);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (s0 + u < nsteps) {
+          const int v = wb + (s0 + u) * 32 + lane;
+          f(head + v * VEC, q[u], v < we ? VEC : 0);
+        }
       }
     }
-    used += (uint32_t)nch;
-    if (has_tail) per_chunk(nch, -1);
-  };
-  auto each_vec = [&](bool last_use, auto&& f) {
-    stream(last_use, [&](int c, int slot) { warp_chunk(c, slot, f); });
+    if (warp == kWarps - 1 && tail > 0) {
+      const int e0 = head + nvec * VEC;
+      const uint4 q = load_partial(e0, lane == 0 ? tail : 0);
+      f(e0, q, lane == 0 ? tail : 0);
+    }
   };
   auto each_elem = [&](auto&& g) {
-    each_vec(false, [&](int, const uint4& q, int nv) {
-      const raw* r = reinterpret_cast<const raw*>(&q);
+    sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
 #pragma unroll
       for (int j = 0; j < VEC; ++j)
-        if (j < nv) g(r[j]);
+        if (j < nv) g(vec_elem<DT>(q, j));
     });
   };
 
-  // bit j set when element j (of nv) is >= the value whose lanes fill B2
+  // bit j set when element j (of nv) is >= / == the value whose lanes fill B2
   auto ge_bits = [&](const uint4& q, int nv, uint32_t B2) -> uint32_t {
     const uint32_t b = mask_bits<KB>(P::ge(q.x, B2), P::ge(q.y, B2), P::ge(q.z, B2), P::ge(q.w, B2));
     return b & ((1u << nv) - 1u);
@@ -432,93 +400,30 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     return b & ((1u << nv) - 1u);
   };
   // key of the largest element of a vector with at least one valid element
-  // (the -inf padding never wins)
   auto vmax_key = [&](const uint4& q) -> uint32_t { return order_key<DT>((raw)P::max_raw(q)); };
-  // appends the elements flagged in bits to this warp's list (all lanes call it)
-  uint32_t nseg = 0;  // warp-uniform
-  auto append = [&](const uint4& q, uint32_t bits) {
-    const uint32_t c = __popc(bits);
-    if (!__any_sync(0xffffffffu, c != 0)) return;
-    const uint32_t incl = warp_incl_scan(c);
-    uint32_t slot = nseg + incl - c;
-    while (bits) {
-      const int j = __ffs(bits) - 1;
-      bits &= bits - 1;
-      if (slot < (uint32_t)CAPW) seg[slot] = (ckey)order_key<DT>(vec_elem<DT>(q, j));
-      ++slot;
-    }
-    nseg += __shfl_sync(0xffffffffu, incl, 31);
-  };
 
-  // ---- pass A (from HBM): the row max, plus ----
+  // ---- pass A (from HBM): the row max, plus the first-digit histogram ----
   uint32_t kmax = 0;
-  bool listed = false;   // top-k candidates collected during pass A
-  uint32_t Lkey = 0;     // candidate bound
-  if (topk) {
-    // The first kApplySlots chunks stay resident until the k-th largest of
-    // their vector maxima gives the candidate bound L; then every vector of
-    // the row, those chunks included, is tested against L as it passes.
-    const int npre = min(nch, kApplySlots);
-    if (aligned && tid == 0)
-      for (int c = 0; c < npre; ++c) issue(c, false);
-    for (int c = 0; c < npre; ++c) {
-      if (aligned && !mbar_wait_bounded(&h.full[c], 0u, a.timeout_ns)) my_fail = true;
-      warp_chunk(c, c, [&](int, const uint4& q, int nv) {
-        if (nv) {
-          const uint32_t key = vmax_key(q);
-          kmax = max(kmax, key);
-          atomicAdd(&hist[key >> SHB], 1u);
-        }
-      });
-    }
-    __syncthreads();
-    const int lb = select_desc_f<kBins / kThreads>(
-        [&](int j) -> unsigned long long { return hist[(kBins / kThreads) * tid + j]; }, (unsigned long long)kv, h).bin;
-    listed = lb >= 0;
-    Lkey = listed ? (uint32_t)lb << SHB : 0u;
-    const uint32_t L2 = P::splat((uint32_t)raw_of_key<DT>(Lkey));
-    auto step_rest = [&](const uint4& q, int nv) {
+  if (topk && !generic_only) {
+    // of the vector maxima
+    sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) {
       if (nv) {
         const uint32_t key = vmax_key(q);
         kmax = max(kmax, key);
-        if (!listed) atomicAdd(&hist[key >> SHB], 1u);
+        atomicAdd(&hist[key >> SHB], 1u);
       }
-      if (listed) append(q, nv ? ge_bits(q, nv, L2) : 0u);
-    };
-    for (int c = 0; c < npre; ++c) {
-      if (listed) warp_chunk(c, c, [&](int, const uint4& q, int nv) { append(q, nv ? ge_bits(q, nv, L2) : 0u); });
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&h.empty[c]);
-      if (aligned && tid == 0 && c + kApplySlots < nch) {
-        fence_proxy_async_shared();
-        issue(c + kApplySlots, false);
-      }
-    }
-    for (int c = npre; c < nch; ++c) {
-      const int slot = c % kApplySlots;
-      if (aligned && !mbar_wait_bounded(&h.full[slot], (uint32_t)(c / kApplySlots) & 1u, a.timeout_ns))
-        my_fail = true;
-      warp_chunk(c, slot, [&](int, const uint4& q, int nv) { step_rest(q, nv); });
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&h.empty[slot]);
-      if (aligned && tid == 0 && c + kApplySlots < nch) {
-        fence_proxy_async_shared();
-        issue(c + kApplySlots, false);
-      }
-    }
-    used = (uint32_t)nch;
-    if (has_tail) warp_chunk(nch, -1, [&](int, const uint4& q, int nv) { step_rest(q, nv); });
-  } else if (!keepall) {
-    // the per-bucket counts of every element (window path)
-    each_vec(false, [&](int, const uint4& q, int nv) {
+    });
+  } else if (window) {
+    // of every element
+    sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
+      if (nv) kmax = max(kmax, vmax_key(q));
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        if (j < nv) {
-          const uint32_t key = order_key<DT>(vec_elem<DT>(q, j));
-          kmax = max(kmax, key);
-          if (window) atomicAdd(&hist[key >> SHB], 1u);
-        }
-      }
+      for (int j = 0; j < VEC; ++j)
+        if (j < nv) atomicAdd(&hist[order_key<DT>(vec_elem<DT>(q, j)) >> SHB], 1u);
+    });
+  } else if (!keepall) {
+    sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) {
+      if (nv) kmax = max(kmax, vmax_key(q));
     });
   }
   kmax = __reduce_max_sync(0xffffffffu, kmax);
@@ -529,26 +434,35 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   unsigned long long r0 = 0;    // ties of T masked, in index order
   bool cut_last = false;        // top-p keeps only the last sorted position
   bool done = keepall;          // cut found
+  bool have_wtie = false;       // h.wtie holds the ties of T per warp
   const float thr = topp ? top_p_threshold<DT>(a.p, row) : 0.0f;
   const uint32_t gmax = h.maxkey;
   const MassRef mr(value_of_key<DT>(gmax));
 
   // ---------------------------------------------------- candidate path
-  if (topk) {
-    bool have = listed;
-    if (!listed) {
-      // k exceeds the resident vectors: bound from the whole row's vector
-      // maxima, then pass B (from L2) collects the candidates
-      const int lb = select_desc_f<kBins / kThreads>(
-          [&](int j) -> unsigned long long { return hist[(kBins / kThreads) * tid + j]; }, (unsigned long long)kv, h).bin;
-      if (lb >= 0) {
-        Lkey = (uint32_t)lb << SHB;
-        const uint32_t L2 = P::splat((uint32_t)raw_of_key<DT>(Lkey));
-        each_vec(false, [&](int, const uint4& q, int nv) { append(q, nv ? ge_bits(q, nv, L2) : 0u); });
-        have = true;
-      }
-    }
-    if (have) {
+  if (topk && !generic_only) {
+    const int lb = select_desc_f<kBins / kThreads>(
+        [&](int j) -> unsigned long long { return hist[(kBins / kThreads) * tid + j]; }, (unsigned long long)kv, h).bin;
+    if (lb > 0) {
+      // pass B (from L2): every element >= L joins its warp's list
+      const uint32_t Lkey = (uint32_t)lb << SHB;
+      const uint32_t L2 = P::splat((uint32_t)raw_of_key<DT>(Lkey));
+      uint32_t nseg = 0;  // warp-uniform
+      sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) {
+        const bool cand = nv != 0 && (P::ge(q.x, L2) | P::ge(q.y, L2) | P::ge(q.z, L2) | P::ge(q.w, L2)) != 0u;
+        if (!__any_sync(0xffffffffu, cand)) return;
+        uint32_t bits = cand ? ge_bits(q, nv, L2) : 0u;
+        const uint32_t c = __popc(bits);
+        const uint32_t incl = warp_incl_scan(c);
+        uint32_t slot = nseg + incl - c;
+        while (bits) {
+          const int j = __ffs(bits) - 1;
+          bits &= bits - 1;
+          if (slot < (uint32_t)CAPW) seg[slot] = (ckey)order_key<DT>(vec_elem<DT>(q, j));
+          ++slot;
+        }
+        nseg += __shfl_sync(0xffffffffu, incl, 31);
+      });
       if (lane == 0) {
         h.nseg[warp] = min(nseg, (uint32_t)CAPW);
         if (nseg > (uint32_t)CAPW) h.over = 1;
@@ -651,6 +565,12 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         }
         if (cut_last) T = gmax;
         done = true;
+        // ties of T per warp, from the lists (T >= L is listed)
+        uint32_t ct = 0;
+        each_own([&](uint32_t key) { ct += (key == T); });
+        ct = __reduce_add_sync(0xffffffffu, ct);
+        if (lane == 0) h.wtie[warp] = ct;
+        have_wtie = true;
       }
     }
   }
@@ -689,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       for (int i = lane; i < kWinKeys; i += 32) whist[i] = 0;
       __syncwarp();
       unsigned long long s_mine = 0, b_mine = 0;
-      each_vec(false, [&](int, const uint4& q, int nv) {
+      sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
         float sv = 0.0f, bv = 0.0f;
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
@@ -712,25 +632,27 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         // only the last sorted position survives: the last element equal to the max
         cut_last = true;
         T = gmax;
-        uint32_t cm = 0;
-        each_elem([&](raw r) { cm += (order_key<DT>(r) == gmax); });
-        r0 = block_sum(cm, h.ws) - 1ull;
         done = true;
       } else if (target >= below) {
-        // window keys, one per thread: counts summed over the warps
-        unsigned long long wb[1] = {0};
-        if (tid < nwin) {
-          const uint32_t* allw = reinterpret_cast<const uint32_t*>(big);
+        // window keys, BPTW per thread: counts summed over the warps
+        constexpr int BPTW = kWinKeys / kThreads;
+        static_assert(BPTW * kThreads == kWinKeys, "window keys split evenly over the threads");
+        const uint32_t* allw = reinterpret_cast<const uint32_t*>(big);
+        auto wm = [&](int j) -> unsigned long long {
+          const int key = BPTW * tid + j;
+          if (key >= nwin) return 0ull;
           unsigned long long cw = 0;
-          for (int w = 0; w < kApplyWarps; ++w) cw += allw[w * kWinKeys + tid];
-          wb[0] = cw ? cw * mass_fixed(value_of_key<DT>(wkey0 + tid), mr) : 0ull;
-        }
-        const Sel sw2 = select_asc(wb, target - below, h);
+          for (int w = 0; w < kWarps; ++w) cw += allw[w * kWinKeys + key];
+          return cw ? cw * mass_fixed(value_of_key<DT>(wkey0 + (uint32_t)key), mr) : 0ull;
+        };
+        const Sel sw2 = select_asc_f<BPTW>(wm, target - below, h);
         if (sw2.bin >= 0) {
           T = wkey0 + (uint32_t)sw2.bin;
           const unsigned long long u = mass_fixed(value_of_key<DT>(T), mr);
           r0 = u ? (target - below - sw2.off) / u : 0ull;
           done = true;
+          if (lane == 0) h.wtie[warp] = whist[T - wkey0];
+          have_wtie = true;
         }
       }
     }
@@ -818,128 +740,103 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         r0 = u ? rem / u : 0ull;
       }
     }
-    if (cut_last) {
-      T = gmax;
-      uint32_t cm = 0;
-      each_elem([&](raw r) { cm += (order_key<DT>(r) == gmax); });
-      r0 = block_sum(cm, h.ws) - 1ull;
-    }
+    if (cut_last) T = gmax;
   }
-  if (my_fail) atomicOr(&h.failed, 1u);
+
+  // ---- ties of T per warp, where the path did not count them ----
+  const uint32_t T2 = P::splat((uint32_t)raw_of_key<DT>(T));
+  if (!keepall && (cut_last || r0 > 0) && !have_wtie) {
+    uint32_t ct = 0;
+    sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) { ct += __popc(eq_bits(q, nv, T2)); });
+    ct = __reduce_add_sync(0xffffffffu, ct);
+    if (lane == 0) h.wtie[warp] = ct;
+  }
   __syncthreads();
+  if (cut_last) {
+    // only the last sorted position survives: the last element equal to the max
+    unsigned long long all = 0;
+    for (int w = 0; w < kWarps; ++w) all += h.wtie[w];
+    r0 = all - 1ull;
+  }
 
   // ---- write pass: original element or -inf, in original order ([guide] §2 step 8) ----
-  const bool skip_writes = h.failed != 0;
-  const uint32_t T2 = P::splat((uint32_t)raw_of_key<DT>(T));
-  const bool vec_store = a.vec_out != 0;
-  auto put = [&](int e, const uint4& q, int nv) {
-    if (skip_writes || my_fail || nv == 0) return;  // a timed-out slot holds stale data
-    if (nv == VEC && vec_store) {
-      st_global_hint(orow + e, q, pol_last);
+  int rule = kKeepAll;
+  unsigned long long seen = 0;  // ties of T before this warp's next vector (straddling warp)
+  if (!keepall) {
+    if (r0 == 0) {
+      rule = kTiesKept;
     } else {
-      const raw* r = reinterpret_cast<const raw*>(&q);
+      unsigned long long pre = 0;
+      for (int w = 0; w < warp; ++w) pre += h.wtie[w];
+      const unsigned long long mine = h.wtie[warp];
+      rule = (pre + mine <= r0) ? kTiesMasked : (pre >= r0 ? kTiesKept : kTiesStraddle);
+      seen = pre;
+    }
+  }
+  sweep(Loads<kLoadsSimple>{}, true, [&](int e, const uint4& qin, int nv) {
+    uint32_t keep_ties = 0;  // rule == kTiesStraddle: ties of this vector that stay
+    if (rule == kTiesStraddle) {
+      uint32_t tb = eq_bits(qin, nv, T2);
+      const uint32_t cnt = __popc(tb);
+      if (__any_sync(0xffffffffu, cnt != 0)) {
+        const uint32_t incl = warp_incl_scan(cnt);
+        unsigned long long rank = seen + incl - cnt;
+        while (tb) {
+          const int j = __ffs(tb) - 1;
+          tb &= tb - 1;
+          if (rank >= r0) keep_ties |= 1u << j;
+          ++rank;
+        }
+        seen += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+    if (nv == 0) return;
+    uint4 q = qin;
+    if (rule != kKeepAll) {
+      auto fix = [&](uint32_t w, int j) -> uint32_t {
+        uint32_t mk;
+        if (rule == kTiesKept) mk = P::ge(w, T2);
+        else if (rule == kTiesMasked) mk = P::gt(w, T2);
+        else mk = P::gt(w, T2) | bits_word_mask<KB>(keep_ties, j);
+        return (w & mk) | (NEG2 & ~mk);
+      };
+      q.x = fix(q.x, 0);
+      q.y = fix(q.y, 1);
+      q.z = fix(q.z, 2);
+      q.w = fix(q.w, 3);
+    }
+    if (nv == VEC && vec_out) {
+      st_global_hint(orow + e, q, pol_first);
+    } else {
 #pragma unroll
       for (int j = 0; j < VEC; ++j)
-        if (j < nv) orow[e + j] = r[j];
+        if (j < nv) orow[e + j] = vec_elem<DT>(q, j);
     }
-  };
-  const int wrule = keepall ? kKeepAll : (r0 == 0 ? kTiesKept : kTiesStraddle);
-  if (wrule != kTiesStraddle) {
-    each_vec(true, [&](int e, const uint4& qin, int nv) {
-      uint4 q = qin;
-      if (wrule == kTiesKept) {
-        uint32_t* wv = reinterpret_cast<uint32_t*>(&q);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t mk = P::ge(wv[j], T2);
-          wv[j] = (wv[j] & mk) | (NEG2 & ~mk);
-        }
-      }
-      put(e, q, nv);
-    });
-  } else {
-    // The cut falls inside the run of elements equal to T: the first r0 of
-    // them, in index order, are masked.  Per chunk, a scan over the warps'
-    // tie counts tells each warp whether its ties are all masked, all kept,
-    // or (one warp of one chunk) split, which it resolves with warp scans.
-    unsigned long long running = 0;  // ties in earlier chunks (CTA-uniform)
-    stream(true, [&](int c, int slot) {
-      uint32_t wc = 0;
-      warp_chunk(c, slot, [&](int, const uint4& q, int nv) { wc += __popc(eq_bits(q, nv, T2)); });
-      wc = __reduce_add_sync(0xffffffffu, wc);
-      const int par = (c & 1);
-      if (lane == 0) h.wtie[par][warp] = wc;
-      __syncthreads();
-      unsigned long long pre = running, tot = 0;
-      for (int w = 0; w < kApplyWarps; ++w) {
-        if (w < warp) pre += h.wtie[par][w];
-        tot += h.wtie[par][w];
-      }
-      const int rl = (pre + wc <= r0) ? kTiesMasked : (pre >= r0 ? kTiesKept : kTiesStraddle);
-      unsigned long long seen = pre;  // warp-uniform
-      warp_chunk(c, slot, [&](int e, const uint4& qin, int nv) {
-        uint4 q = qin;
-        uint32_t keep_ties = 0;  // rl == kTiesStraddle: ties of this vector that stay
-        if (rl == kTiesStraddle) {
-          uint32_t tb = eq_bits(q, nv, T2);
-          const uint32_t cnt = __popc(tb);
-          const uint32_t incl = warp_incl_scan(cnt);
-          unsigned long long rank = seen + incl - cnt;
-          while (tb) {
-            const int j = __ffs(tb) - 1;
-            tb &= tb - 1;
-            if (rank >= r0) keep_ties |= 1u << j;
-            ++rank;
-          }
-          seen += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        uint32_t* wv = reinterpret_cast<uint32_t*>(&q);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t mk;
-          if (rl == kTiesKept) mk = P::ge(wv[j], T2);
-          else if (rl == kTiesMasked) mk = P::gt(wv[j], T2);
-          else mk = P::gt(wv[j], T2) | bits_word_mask<KB>(keep_ties, j);
-          wv[j] = (wv[j] & mk) | (NEG2 & ~mk);
-        }
-        put(e, q, nv);
-      });
-      running += tot;
-    });
-  }
-  if (my_fail) atomicOr(&g_device_error, 1u);
+  });
 }
 
 template <int DT>
-static cudaError_t launch_one(const ApplyPlan& plan, const ApplyArgs& a, cudaStream_t s) {
+static cudaError_t launch_one(const ApplyArgs& a, cudaStream_t s) {
   auto kern = apply_kernel<DT>;
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kApplySmem);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  kern<<<dim3((unsigned)a.B), dim3(kThreads), plan.smem, s>>>(a);
+  kern<<<dim3((unsigned)a.B), dim3(kThreads), kApplySmem, s>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_apply(topkp_dtype dt, const ApplyPlan& plan, const ApplyArgs& a, cudaStream_t s) {
+cudaError_t launch_apply(topkp_dtype dt, const ApplyArgs& a, cudaStream_t s) {
   switch (dt) {
-    case TOPKP_F32: return launch_one<TOPKP_F32>(plan, a, s);
-    case TOPKP_F16: return launch_one<TOPKP_F16>(plan, a, s);
-    case TOPKP_BF16: return launch_one<TOPKP_BF16>(plan, a, s);
+    case TOPKP_F32: return launch_one<TOPKP_F32>(a, s);
+    case TOPKP_F16: return launch_one<TOPKP_F16>(a, s);
+    case TOPKP_BF16: return launch_one<TOPKP_BF16>(a, s);
   }
   return cudaErrorInvalidValue;
-}
-
-// Reads and clears this translation unit's device error word.
-cudaError_t apply_take_device_error(unsigned int* out) {
-  cudaError_t e = cudaMemcpyFromSymbol(out, g_device_error, sizeof(unsigned int));
-  if (e != cudaSuccess) return e;
-  const unsigned int zero = 0;
-  return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned int));
 }
 
 }  // namespace topkp

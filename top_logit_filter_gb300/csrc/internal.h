@@ -9,10 +9,9 @@
 namespace topkp {
 
 // ---------------------------------------------------------------- apply
-// One CTA filters one row.  The row streams through a ring of kApplySlots
-// chunk-sized slots in shared memory, filled by single large bulk copies:
-// once from HBM, then again from L2 for the later passes.  Warp w handles
-// the w-th sixteenth of every chunk.
+// One CTA filters one row.  Warp w owns the w-th sixteenth of the row's
+// 16-byte vectors and reads them straight into registers: once from HBM,
+// then again from L2 for the later passes.
 struct ApplyArgs {
   const void* x;          // logits [B, ldx]
   void* out;              // out [B, ldo]
@@ -21,35 +20,21 @@ struct ApplyArgs {
   int64_t ldx, ldo;       // row strides, elements
   int64_t B;
   int32_t V;
-  int32_t chunk;          // bytes per ring slot (multiple of 8 KB)
-  int32_t aligned;        // rows of x are 16-byte aligned: bulk copies / vector loads
-  int32_t vec_out;        // rows of out are 16-byte aligned: vector stores
-  uint64_t timeout_ns;    // limit of every bounded wait
+  int32_t force;          // kApplyForce* bits (testing: route rows to one path)
 };
 
-struct ApplyPlan {
-  int chunk = 16384;
-  int ctas_per_sm = 2;
-  size_t smem = 0;        // dynamic shared memory per CTA
-};
+// Every row that needs a cut takes the generic radix path.
+constexpr int32_t kApplyForceGeneric = 1;
 
-// Shared memory of one apply CTA: header (mbarriers, small histograms), a
-// 4096-bin histogram, a 24 KB region for the per-warp candidate lists (or
-// per-warp window counts, or generic-path mass bins), then the ring.
-constexpr int kApplyWarps = 16;
-constexpr int kApplySlots = 4;
+// Shared memory of one apply CTA: header (small histograms, scan scratch),
+// a 4096-bin histogram, and a 64 KB region for the per-warp candidate lists
+// (or per-warp window counts, or generic-path mass bins).
 constexpr size_t kApplyHdrBytes = 4096;
 constexpr size_t kApplyHistBytes = 4096 * 4;
-constexpr size_t kApplyBigBytes = 24576;
-constexpr size_t kApplyFixedSmem = kApplyHdrBytes + kApplyHistBytes + kApplyBigBytes;
+constexpr size_t kApplyBigBytes = 65536;
+constexpr size_t kApplySmem = kApplyHdrBytes + kApplyHistBytes + kApplyBigBytes;
 
-inline size_t apply_smem_bytes(int chunk) { return kApplyFixedSmem + (size_t)kApplySlots * chunk; }
-
-cudaError_t launch_apply(topkp_dtype dt, const ApplyPlan& plan, const ApplyArgs& a, cudaStream_t s);
-
-// Chooses the ring slot size and CTAs per SM for a problem on a device with
-// `num_sms` SMs and `l2_bytes` of L2.
-ApplyPlan plan_apply(int64_t B, int64_t V, int esize, int num_sms, int64_t l2_bytes, const char* force);
+cudaError_t launch_apply(topkp_dtype dt, const ApplyArgs& a, cudaStream_t s);
 
 // --------------------------------------------------------------- sorted
 struct SortedArgs {
@@ -78,9 +63,8 @@ struct SortedPlan {
 SortedPlan plan_sorted(int64_t B, int64_t V, int esize, int num_sms, bool with_logits, const char* force);
 cudaError_t launch_sorted(topkp_dtype dt, const SortedPlan& plan, const SortedArgs& a, cudaStream_t s);
 
-// Each kernel translation unit keeps a device error word (bit 0: a bounded
-// wait gave up); these read and clear it (synchronous).
-cudaError_t apply_take_device_error(unsigned int* out);
+// The sorted-path translation unit keeps a device error word (bit 0: a
+// bounded wait gave up); this reads and clears it (synchronous).
 cudaError_t sorted_take_device_error(unsigned int* out);
 
 }  // namespace topkp
