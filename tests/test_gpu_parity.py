@@ -34,6 +34,12 @@ def _rows(rng, B, V, dtype, kind):
         x = rng.standard_normal((B, V)).astype(np.float32) * 3
     elif kind == "ties":
         x = (rng.integers(-6, 7, size=(B, V)) * 0.5).astype(np.float32)
+    elif kind == "wide":
+        # magnitudes over dozens of binades, both signs: a 16-bit row then
+        # touches more key buckets than the key-count path has blocks
+        lo, hi = (-20.0, 14.0) if dtype == "f16" else (-60.0, 60.0)
+        sign = np.where(rng.random((B, V)) < 0.5, -1.0, 1.0)
+        x = (sign * np.exp2(rng.uniform(lo, hi, size=(B, V)))).astype(np.float32)
     else:  # "zeros": signed zeros and a few values
         x = rng.choice(np.array([-0.0, 0.0, 1.0, -1.0, 2.0], dtype=np.float32), size=(B, V))
     return np.stack([to_raw(r, dtype) for r in x])
@@ -75,7 +81,7 @@ PLANS = ["", "generic"]
 def test_small_rows_all_plans(tk, monkeypatch, dtype, V, mode):
     rng = np.random.default_rng(V * 7 + len(mode))
     B = 9
-    for kind in ("normal", "ties", "zeros"):
+    for kind in ("normal", "ties", "zeros", "wide"):
         x = _rows(rng, B, V, dtype, kind)
         k, p = _kp(rng, B, V, dtype, mode)
         for plan in PLANS:
@@ -90,7 +96,7 @@ def test_multi_slice_rows(tk, monkeypatch, dtype):
     partial last warp step and a tail shorter than 16 bytes."""
     rng = np.random.default_rng(3)
     B, V = 6, 40011
-    for kind in ("normal", "ties"):
+    for kind in ("normal", "ties", "wide"):
         x = _rows(rng, B, V, dtype, kind)
         k, p = _kp(rng, B, V, dtype, "kp")
         k[:3] = [0, 37, 900]

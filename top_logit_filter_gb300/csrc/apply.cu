@@ -24,29 +24,32 @@
 //   2. the k-th largest vector maximum lower-bounds the row's k-th largest
 //      element (k distinct elements reach it); its bucket floor L decides
 //      candidacy.  Pass B tests every vector with one packed ">= L" compare
-//      and each warp appends the few elements >= L to its own list;
+//      and appends the few elements >= L to its warp's list;
 //   3. the selection runs on the lists alone: the k-th largest key by counts,
 //      then the top-p cut by probability mass (2^-40 fixed point; for 16-bit
 //      dtypes an exact per-key histogram, so mass = count x exp(value - max)).
 // Rows with top-p only (fp16 / bf16) take the window path:
-//   1. pass A counts every element per first-digit bucket;
+//   1. pass A counts every element per 12-bit bucket;
 //   2. rigorous lower / upper bounds of every bucket's mass (count times the
 //      mass of its smallest / largest value) bracket the top-p cut into a
-//      window of buckets;
+//      window of buckets; each non-empty bucket of the window gets a block of
+//      16 per-key counters (a window that crosses zero spans thousands of
+//      nearly empty buckets, so only occupied ones get counters);
 //   3. pass B computes every element's mass: the row total and the mass
 //      below the window accumulate in registers (fp32 per 16-byte vector,
-//      then 2^-40 fixed point), the window gets exact per-key counts per
-//      warp; the cut follows from count x mass per key.
-// Everything else (fp32 top-p-only rows, candidate overflow, wide windows)
-// takes the generic path: a radix descent over the whole row (11-bit first
-// digit, then 5 bits for 16-bit keys or 11 + 10 for fp32).
+//      then 2^-40 fixed point), the few elements inside the window are
+//      counted per key; the cut follows from count x mass per key.
+// Everything else (fp32 top-p-only rows, overflowing lists, windows with too
+// many occupied buckets) takes the generic path: a radix descent over the
+// whole row (11-bit first digit, then 5 bits for 16-bit keys or 11 + 10 for
+// fp32).
 //
 // When the cut falls inside a run of equal values, the write pass needs each
 // tie's rank in index order.  The ties of T in each warp's sixteenth are
-// known before the write pass (from the warp's candidate list, its window
-// histogram, or a counting pass), so a warp whose ties are all masked or all
-// kept applies one compare; the single warp where the cut falls ranks its
-// ties with warp scans.
+// known before the write pass (from the warp's candidate list or a counting
+// pass), so a warp whose ties are all masked or all kept applies one
+// compare; the single warp where the cut falls ranks its ties with warp
+// scans.
 #include <type_traits>
 
 #include "common.cuh"
@@ -54,14 +57,17 @@
 
 namespace topkp {
 
-constexpr int kBins = 4096;                  // candidate / window path first digit: 12 bits
+constexpr int kBins = 4096;                  // 12-bit first digit: candidate path, key-count buckets
 constexpr int kSmallBins = 256;              // 8-bit digits over candidate lists
-constexpr int kWinKeys = (int)(kApplyBigBytes / 4 / kWarps);  // window keys per warp histogram
+constexpr int kKeyBlocks = (int)(kApplyBigBytes / (16 * 4));  // 16-key count blocks of the window path
+static_assert(kApplyAuxBytes >= (size_t)kKeyBlocks * (2 + 8), "block -> bucket map and block masses");
+static_assert(2 * kBins * 8 <= (int)kApplyBigBytes, "bucket mass bounds fit the big region");
+constexpr uint32_t kNoBlock = 0xffffffffu;   // bucket without a count block
 constexpr int kLoadsSimple = 8;              // vectors in flight per lane, light per-vector work
 constexpr int kLoadsHeavy = 4;               // vectors in flight per lane, per-element work
 
 struct __align__(16) ApplyHdr {
-  unsigned long long ws[kWarps];        // block-scan scratch
+  unsigned long long ws[2 * kWarps];    // block-scan scratch (paired scans use both halves)
   unsigned long long sel_off;           // select result: count/mass outside the bin
   unsigned long long small_mass[kSmallBins];
   uint32_t small_cnt[kSmallBins];
@@ -70,6 +76,7 @@ struct __align__(16) ApplyHdr {
   int sel_bin;                          // select result: bin, -1 if none
   uint32_t maxkey;                      // row max key
   uint32_t over;                        // a candidate list overflowed
+  int w0, w1;                           // window path: first / last bucket of the window
 };
 static_assert(sizeof(ApplyHdr) <= kApplyHdrBytes, "header too large");
 
@@ -91,6 +98,10 @@ template <> struct Levels<32> {
 // Masks are all-ones in every lane (half or word) where the predicate holds.
 template <int DT> struct Packed;
 template <> struct Packed<TOPKP_BF16> {
+  // both values of a word as floats (low half first)
+  __device__ static __forceinline__ float2 unpack2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
   __device__ static __forceinline__ __nv_bfloat162 v2(uint32_t w) { return *reinterpret_cast<__nv_bfloat162*>(&w); }
   __device__ static __forceinline__ uint32_t max_raw(uint4 q) {
     const __nv_bfloat162 m = __hmax2(__hmax2(v2(q.x), v2(q.y)), __hmax2(v2(q.z), v2(q.w)));
@@ -103,6 +114,8 @@ template <> struct Packed<TOPKP_BF16> {
   __device__ static __forceinline__ uint32_t splat(uint32_t raw) { return raw | (raw << 16); }
 };
 template <> struct Packed<TOPKP_F16> {
+  // both values of a word as floats (low half first)
+  __device__ static __forceinline__ float2 unpack2(uint32_t w) { return __half22float2(*reinterpret_cast<__half2*>(&w)); }
   __device__ static __forceinline__ __half2 v2(uint32_t w) { return *reinterpret_cast<__half2*>(&w); }
   __device__ static __forceinline__ uint32_t max_raw(uint4 q) {
     const __half2 m = __hmax2(__hmax2(v2(q.x), v2(q.y)), __hmax2(v2(q.z), v2(q.w)));
@@ -115,6 +128,7 @@ template <> struct Packed<TOPKP_F16> {
   __device__ static __forceinline__ uint32_t splat(uint32_t raw) { return raw | (raw << 16); }
 };
 template <> struct Packed<TOPKP_F32> {
+  __device__ static __forceinline__ float2 unpack2(uint32_t w) { return make_float2(__uint_as_float(w), 0.0f); }
   __device__ static __forceinline__ uint32_t max_raw(uint4 q) {
     return __float_as_uint(fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
                                  fmaxf(__uint_as_float(q.z), __uint_as_float(q.w))));
@@ -153,6 +167,15 @@ __device__ __forceinline__ typename DType<DT>::raw vec_elem(const uint4& q, int 
     return (typename DType<DT>::raw)((j & 1) ? (w >> 16) : (w & 0xffffu));
   }
   return (typename DType<DT>::raw)((j & 2) ? ((j & 1) ? q.w : q.z) : ((j & 1) ? q.y : q.x));
+}
+
+// Order keys of the two 16-bit values in a word, packed the same way (the
+// order_key mapping, two lanes at once: neither lane carries into the other).
+__device__ __forceinline__ uint32_t order_keys2(uint32_t w) {
+  const uint32_t mag = w & 0x7fff7fffu;
+  const uint32_t neg = (w >> 15) & 0x00010001u;
+  const uint32_t m = (neg << 16) - neg;  // 0xffff in every negative lane
+  return ((0x80008000u + mag) & ~m) | ((0x80008000u - mag) & m);
 }
 
 // --------------------------------------------------- block-wide selection
@@ -248,10 +271,7 @@ __device__ __forceinline__ unsigned long long block_sum_f(F&& val, unsigned long
   return block_sum(s, ws);
 }
 
-// masked iff cumulative mass <= thr * S (integers: <= floor(thr * S))
-__device__ __forceinline__ unsigned long long mass_target(float thr, unsigned long long S) {
-  return (unsigned long long)floor((double)thr * (double)S);
-}
+
 
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
   const int lane = threadIdx.x & 31;
@@ -288,7 +308,13 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   ApplyHdr& h = *reinterpret_cast<ApplyHdr*>(smem);
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kApplyHdrBytes);
-  unsigned char* big = smem + kApplyHdrBytes + kApplyHistBytes;
+  unsigned char* aux = smem + kApplyHdrBytes + kApplyHistBytes;
+  unsigned char* big = aux + kApplyAuxBytes;
+  // window path: bucket -> count block, block -> bucket, block masses, counts
+  uint32_t* block_of = hist;
+  uint16_t* bucket_of = reinterpret_cast<uint16_t*>(aux);
+  unsigned long long* block_mass = reinterpret_cast<unsigned long long*>(aux + kKeyBlocks * 2);
+  uint32_t* kcount = reinterpret_cast<uint32_t*>(big);
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -297,7 +323,6 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   const raw* xr = reinterpret_cast<const raw*>(a.x) + row * a.ldx;
   raw* orow = reinterpret_cast<raw*>(a.out) + row * a.ldo;
   ckey* seg = reinterpret_cast<ckey*>(big) + warp * CAPW;
-  uint32_t* whist = reinterpret_cast<uint32_t*>(big) + warp * kWinKeys;
   unsigned long long* mass = reinterpret_cast<unsigned long long*>(big);
 
   const bool generic_only = (a.force & kApplyForceGeneric) != 0;
@@ -327,7 +352,10 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     h.maxkey = 0;
     h.over = 0;
     h.sel_bin = -1;
+    h.w0 = kBins - 1;
+    h.w1 = kBins - 1;
   }
+  if (tid < kWarps) h.nseg[tid] = 0;
   if ((topk && !generic_only) || window)
     for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
   __syncthreads();
@@ -402,10 +430,11 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   // key of the largest element of a vector with at least one valid element
   auto vmax_key = [&](const uint4& q) -> uint32_t { return order_key<DT>((raw)P::max_raw(q)); };
 
-  // ---- pass A (from HBM): the row max, plus the first-digit histogram ----
+  // ---- pass A (from HBM): the row max, plus the 12-bit first-digit
+  // histogram of the vector maxima (candidate path) or of every element
+  // (window path) ----
   uint32_t kmax = 0;
   if (topk && !generic_only) {
-    // of the vector maxima
     sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) {
       if (nv) {
         const uint32_t key = vmax_key(q);
@@ -414,13 +443,17 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       }
     });
   } else if (window) {
-    // of every element
-    sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
-      if (nv) kmax = max(kmax, vmax_key(q));
+    if constexpr (KB == 16) {
+      sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
+        if (nv) kmax = max(kmax, vmax_key(q));
+        const uint32_t kp[4] = {order_keys2(q.x), order_keys2(q.y), order_keys2(q.z), order_keys2(q.w)};
 #pragma unroll
-      for (int j = 0; j < VEC; ++j)
-        if (j < nv) atomicAdd(&hist[order_key<DT>(vec_elem<DT>(q, j)) >> SHB], 1u);
-    });
+        for (int j = 0; j < VEC; ++j) {
+          const uint32_t key = (j & 1) ? (kp[j >> 1] >> 16) : (kp[j >> 1] & 0xffffu);
+          if (j < nv) atomicAdd(&hist[key >> SHB], 1u);
+        }
+      });
+    }
   } else if (!keepall) {
     sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) {
       if (nv) kmax = max(kmax, vmax_key(q));
@@ -435,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   bool cut_last = false;        // top-p keeps only the last sorted position
   bool done = keepall;          // cut found
   bool have_wtie = false;       // h.wtie holds the ties of T per warp
+  bool r0_known = true;         // cut_last: r0 already counted
   const float thr = topp ? top_p_threshold<DT>(a.p, row) : 0.0f;
   const uint32_t gmax = h.maxkey;
   const MassRef mr(value_of_key<DT>(gmax));
@@ -447,25 +481,22 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       // pass B (from L2): every element >= L joins its warp's list
       const uint32_t Lkey = (uint32_t)lb << SHB;
       const uint32_t L2 = P::splat((uint32_t)raw_of_key<DT>(Lkey));
-      uint32_t nseg = 0;  // warp-uniform
       sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) {
-        const bool cand = nv != 0 && (P::ge(q.x, L2) | P::ge(q.y, L2) | P::ge(q.z, L2) | P::ge(q.w, L2)) != 0u;
-        if (!__any_sync(0xffffffffu, cand)) return;
-        uint32_t bits = cand ? ge_bits(q, nv, L2) : 0u;
-        const uint32_t c = __popc(bits);
-        const uint32_t incl = warp_incl_scan(c);
-        uint32_t slot = nseg + incl - c;
-        while (bits) {
-          const int j = __ffs(bits) - 1;
-          bits &= bits - 1;
-          if (slot < (uint32_t)CAPW) seg[slot] = (ckey)order_key<DT>(vec_elem<DT>(q, j));
-          ++slot;
+        if (nv != 0 && (P::ge(q.x, L2) | P::ge(q.y, L2) | P::ge(q.z, L2) | P::ge(q.w, L2)) != 0u) {
+          uint32_t bits = ge_bits(q, nv, L2);
+          uint32_t slot = atomicAdd(&h.nseg[warp], (uint32_t)__popc(bits));
+          while (bits) {
+            const int j = __ffs(bits) - 1;
+            bits &= bits - 1;
+            if (slot < (uint32_t)CAPW) seg[slot] = (ckey)order_key<DT>(vec_elem<DT>(q, j));
+            ++slot;
+          }
         }
-        nseg += __shfl_sync(0xffffffffu, incl, 31);
       });
-      if (lane == 0) {
-        h.nseg[warp] = min(nseg, (uint32_t)CAPW);
-        if (nseg > (uint32_t)CAPW) h.over = 1;
+      __syncwarp();
+      if (lane == 0 && h.nseg[warp] > (uint32_t)CAPW) {
+        h.nseg[warp] = CAPW;
+        h.over = 1;
       }
       __syncthreads();
 
@@ -577,82 +608,200 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
 
   // ------------------------------------------------------- window path
   if (window) {
-    constexpr int BPT = kBins / kThreads;
+    constexpr int BPT = kBins / kThreads;  // thread t owns buckets BPT*t .. BPT*t+BPT-1
+    unsigned long long* lo_m = reinterpret_cast<unsigned long long*>(big);  // [kBins]
+    unsigned long long* hi_m = lo_m + kBins;                                // [kBins]
     // rigorous bounds of each bucket's mass: counts times the mass of the
     // bucket's smallest / largest value, widened by 2^-20 and one unit
-    auto lo = [&](int j) -> unsigned long long {
-      const int b = BPT * tid + j;
-      if (!hist[b]) return 0ull;
-      const unsigned long long m0 = mass_fixed(value_of_key<DT>((uint32_t)b << SHB), mr);
-      return hist[b] * (m0 - (m0 >> 20));
-    };
-    auto hi = [&](int j) -> unsigned long long {
-      const int b = BPT * tid + j;
-      if (!hist[b]) return 0ull;
-      const unsigned long long m1 = mass_fixed(value_of_key<DT>(((uint32_t)b << SHB) | ((1u << SHB) - 1u)), mr);
-      return hist[b] * (m1 + (m1 >> 20) + 1);
-    };
-    const unsigned long long SL = block_sum_f<BPT>(lo, h.ws), SU = block_sum_f<BPT>(hi, h.ws);
-    const Sel s0 = select_asc_f<BPT>(hi, mass_target(thr, SL), h);
-    const Sel s1 = select_asc_f<BPT>(lo, mass_target(thr, SU), h);
-    int w0 = s0.bin < 0 ? kBins - 1 : s0.bin;
-    int w1 = s1.bin < 0 ? kBins - 1 : s1.bin;
-    if (thr >= 1.0f) w0 = w1 = (int)(gmax >> SHB);  // only the last position survives
-    const int nwin = (w1 - w0 + 1) << SHB;
-    if (w1 >= w0 && nwin <= kWinKeys) {
-      // pass B (from L2): row mass and mass below the window (fp32 per
-      // vector, then fixed point), per-key window counts per warp.  Window
-      // membership is a float compare: key order is value order.
-      const uint32_t wkey0 = (uint32_t)w0 << SHB;
-      const float lo_f = value_of_key<DT>(wkey0);
-      const float hi_f = value_of_key<DT>(((uint32_t)w1 << SHB) | ((1u << SHB) - 1u));
-      for (int i = lane; i < kWinKeys; i += 32) whist[i] = 0;
-      __syncwarp();
-      unsigned long long s_mine = 0, b_mine = 0;
-      sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
-        float sv = 0.0f, bv = 0.0f;
+    unsigned long long sl = 0, su = 0;
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-          if (j < nv) {
-            const raw rj = vec_elem<DT>(q, j);
-            const float x = D::to_float(rj);
-            const float ej = mass_f32(x, mr);
-            sv += ej;
-            if (x < lo_f) bv += ej;
-            else if (x <= hi_f) atomicAdd(&whist[order_key<DT>(rj) - wkey0], 1u);
+    for (int j = 0; j < BPT; ++j) {
+      const int b = BPT * tid + j;
+      const uint32_t c = hist[b];
+      unsigned long long lo = 0, hi = 0;
+      if (c) {
+        const unsigned long long m0 = mass_fixed(value_of_key<DT>((uint32_t)b << SHB), mr);
+        const unsigned long long m1 = mass_fixed(value_of_key<DT>(((uint32_t)b << SHB) | ((1u << SHB) - 1u)), mr);
+        lo = c * (m0 - (m0 >> 20));
+        hi = c * (m1 + (m1 >> 20) + 1);
+      }
+      lo_m[b] = lo;
+      hi_m[b] = hi;
+      sl += lo;
+      su += hi;
+    }
+    unsigned long long exl, exh, SL, SU;
+    block_exclusive_scan2(sl, su, &exl, &exh, &SL, &SU, h.ws);
+    // the cut's bucket lies between the first bucket whose upper-bound
+    // cumulative mass passes the smallest possible target, and the first
+    // whose lower-bound cumulative mass passes the largest possible one
+    const unsigned long long tL = mass_target(thr, SL), tU = mass_target(thr, SU);
+    if (exh <= tL && tL < exh + su) {
+      unsigned long long acc = exh;
+      for (int j = 0; j < BPT; ++j) {
+        const int b = BPT * tid + j;
+        if (tL < acc + hi_m[b]) {
+          h.w0 = b;
+          break;
+        }
+        acc += hi_m[b];
+      }
+    }
+    if (exl <= tU && tU < exl + sl) {
+      unsigned long long acc = exl;
+      for (int j = 0; j < BPT; ++j) {
+        const int b = BPT * tid + j;
+        if (tU < acc + lo_m[b]) {
+          h.w1 = b;
+          break;
+        }
+        acc += lo_m[b];
+      }
+    }
+    __syncthreads();
+    int w0 = h.w0, w1 = h.w1;
+    if (thr >= 1.0f) w0 = w1 = (int)(gmax >> SHB);  // only the last position survives
+    // 16 per-key counters per window bucket: every bucket of the window in
+    // order when they all fit (a counter's index is then key - first key of
+    // the window), else only the occupied ones (a window that crosses zero
+    // spans thousands of nearly empty buckets)
+    const bool direct = w1 >= w0 && (w1 - w0 + 1) <= kKeyBlocks;
+    uint32_t occ = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+      const int b = BPT * tid + j;
+      occ += (b >= w0 && b <= w1 && (direct || hist[b] != 0)) ? 1u : 0u;
+    }
+    unsigned long long nocc;
+    uint32_t id = (uint32_t)block_exclusive_scan(occ, &nocc, h.ws);
+    if (w1 >= w0 && nocc <= (unsigned long long)kKeyBlocks) {
+#pragma unroll
+      for (int j = 0; j < BPT; ++j) {
+        const int b = BPT * tid + j;
+        if (b >= w0 && b <= w1 && (direct || hist[b] != 0)) {
+          bucket_of[id] = (uint16_t)b;
+          block_of[b] = id++;
+        } else {
+          block_of[b] = kNoBlock;
+        }
+      }
+      uint4* kc4 = reinterpret_cast<uint4*>(kcount);
+      for (int i = tid; i < (int)nocc * 4; i += kThreads) kc4[i] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+      const uint32_t wkey0 = (uint32_t)w0 << SHB;
+      // pass B (from L2): row mass and mass below the window (fp32 per
+      // vector, then fixed point), per-key counts inside the window.  Window
+      // membership is a float compare: key order is value order.
+      const float lo_f = value_of_key<DT>((uint32_t)w0 << SHB);
+      const float hi_f = value_of_key<DT>(((uint32_t)w1 << SHB) | ((1u << SHB) - 1u));
+      unsigned long long s_mine = 0, b_mine = 0;
+      float s_run = 0.0f, b_run = 0.0f;  // fp32 over up to kRun vectors, then fixed point
+      int n_run = 0;
+      constexpr int kRun = 4;
+      const uint32_t LO2 = P::splat((uint32_t)raw_of_key<DT>((uint32_t)w0 << SHB));
+      const uint32_t HI2 = P::splat((uint32_t)raw_of_key<DT>(((uint32_t)w1 << SHB) | ((1u << SHB) - 1u)));
+      sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
+        // two values per word: one packed fma, two exponentials, one packed
+        // add; the -inf padding has zero mass, so no element mask is needed
+        float2 sv = make_float2(0.0f, 0.0f);
+        float bv = 0.0f;
+        const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+        uint32_t wm[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 x = P::unpack2(wd[i]);
+          const float2 e = mass2_f32(x, mr);
+          sv = add2_f32(sv, e);
+          if (x.x < lo_f) bv += e.x;
+          if (x.y < lo_f) bv += e.y;
+          wm[i] = P::ge(wd[i], LO2) & ~P::gt(wd[i], HI2);
+        }
+        s_run += sv.x + sv.y;
+        b_run += bv;
+        if (++n_run == kRun) {
+          s_mine += f2ull_rn(s_run * kMassScaleF);
+          b_mine += f2ull_rn(b_run * kMassScaleF);
+          s_run = b_run = 0.0f;
+          n_run = 0;
+        }
+        // the few elements inside the window: independent, predicated counts
+        const uint32_t inwin = mask_bits<KB>(wm[0], wm[1], wm[2], wm[3]) & ((1u << nv) - 1u);
+        if (inwin) {
+          const uint32_t kp[4] = {order_keys2(wd[0]), order_keys2(wd[1]), order_keys2(wd[2]), order_keys2(wd[3])};
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) {
+            if (inwin & (1u << j)) {
+              const uint32_t key = (j & 1) ? (kp[j >> 1] >> 16) : (kp[j >> 1] & 0xffffu);
+              atomicAdd(&kcount[direct ? key - wkey0 : block_of[key >> SHB] * 16 + (key & 15u)], 1u);
+            }
           }
         }
-        s_mine += __float2ull_rn(sv * kMassScaleF);
-        b_mine += __float2ull_rn(bv * kMassScaleF);
       });
-      const unsigned long long S = block_sum(s_mine, h.ws);
-      const unsigned long long below = block_sum(b_mine, h.ws);
+      s_mine += f2ull_rn(s_run * kMassScaleF);
+      b_mine += f2ull_rn(b_run * kMassScaleF);
+      unsigned long long d0, d1, S, below;
+      block_exclusive_scan2(s_mine, b_mine, &d0, &d1, &S, &below, h.ws);
       const unsigned long long target = mass_target(thr, S);
       if (target >= S) {
         // only the last sorted position survives: the last element equal to the max
         cut_last = true;
         T = gmax;
+        r0_known = false;
         done = true;
       } else if (target >= below) {
-        // window keys, BPTW per thread: counts summed over the warps
-        constexpr int BPTW = kWinKeys / kThreads;
-        static_assert(BPTW * kThreads == kWinKeys, "window keys split evenly over the threads");
-        const uint32_t* allw = reinterpret_cast<const uint32_t*>(big);
-        auto wm = [&](int j) -> unsigned long long {
-          const int key = BPTW * tid + j;
-          if (key >= nwin) return 0ull;
-          unsigned long long cw = 0;
-          for (int w = 0; w < kWarps; ++w) cw += allw[w * kWinKeys + key];
-          return cw ? cw * mass_fixed(value_of_key<DT>(wkey0 + (uint32_t)key), mr) : 0ull;
-        };
-        const Sel sw2 = select_asc_f<BPTW>(wm, target - below, h);
-        if (sw2.bin >= 0) {
-          T = wkey0 + (uint32_t)sw2.bin;
-          const unsigned long long u = mass_fixed(value_of_key<DT>(T), mr);
-          r0 = u ? (target - below - sw2.off) / u : 0ull;
+        // mass of every window key: one block per 16 lanes
+        const uint32_t nblk = (uint32_t)nocc;
+        for (uint32_t base = (uint32_t)warp * 2; base < nblk; base += 2 * kWarps) {
+          const uint32_t blk = base + (uint32_t)(lane >> 4);
+          unsigned long long m = 0;
+          if (blk < nblk) {
+            const uint32_t key = ((uint32_t)bucket_of[blk] << SHB) | (uint32_t)(lane & 15);
+            const uint32_t c = kcount[blk * 16 + (lane & 15)];
+            if (c) m = (unsigned long long)c * mass_fixed(value_of_key<DT>(key), mr);
+          }
+#pragma unroll
+          for (int o = 8; o >= 1; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
+          if (blk < nblk && (lane & 15) == 0) block_mass[blk] = m;
+        }
+        __syncthreads();
+        unsigned long long mb[BPT], sm = 0, tot;
+#pragma unroll
+        for (int j = 0; j < BPT; ++j) {
+          const uint32_t blk = block_of[BPT * tid + j];
+          mb[j] = blk < (uint32_t)kKeyBlocks ? block_mass[blk] : 0ull;
+          sm += mb[j];
+        }
+        const unsigned long long ex = block_exclusive_scan(sm, &tot, h.ws);
+        const unsigned long long tw = target - below;  // mass of the window masked
+        if (ex <= tw && tw < ex + sm) {
+          unsigned long long acc = ex;
+          for (int j = 0; j < BPT; ++j) {
+            if (tw < acc + mb[j]) {
+              const uint32_t b = (uint32_t)(BPT * tid + j);
+              const uint32_t* cb = kcount + block_of[b] * 16;
+              for (int kk = 0; kk < 16; ++kk) {
+                const uint32_t c = cb[kk];
+                if (!c) continue;
+                const uint32_t key = (b << SHB) | (uint32_t)kk;
+                const unsigned long long u = mass_fixed(value_of_key<DT>(key), mr);
+                const unsigned long long mk = (unsigned long long)c * u;
+                if (tw < acc + mk) {
+                  h.sel_bin = (int)key;
+                  h.sel_off = u ? (tw - acc) / u : 0ull;
+                  break;
+                }
+                acc += mk;
+              }
+              break;
+            }
+            acc += mb[j];
+          }
+        }
+        const Sel sp = finish_select(h);
+        if (sp.bin >= 0) {
+          T = (uint32_t)sp.bin;
+          r0 = sp.off;
           done = true;
-          if (lane == 0) h.wtie[warp] = whist[T - wkey0];
-          have_wtie = true;
         }
       }
     }
@@ -740,19 +889,22 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         r0 = u ? rem / u : 0ull;
       }
     }
-    if (cut_last) T = gmax;
+    if (cut_last) {
+      T = gmax;
+      r0_known = false;
+    }
   }
 
   // ---- ties of T per warp, where the path did not count them ----
   const uint32_t T2 = P::splat((uint32_t)raw_of_key<DT>(T));
-  if (!keepall && (cut_last || r0 > 0) && !have_wtie) {
+  if (!keepall && (r0 > 0 || !r0_known) && !have_wtie) {
     uint32_t ct = 0;
     sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) { ct += __popc(eq_bits(q, nv, T2)); });
     ct = __reduce_add_sync(0xffffffffu, ct);
     if (lane == 0) h.wtie[warp] = ct;
   }
   __syncthreads();
-  if (cut_last) {
+  if (!r0_known) {
     // only the last sorted position survives: the last element equal to the max
     unsigned long long all = 0;
     for (int w = 0; w < kWarps; ++w) all += h.wtie[w];

@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "topkp.h"
 
@@ -19,8 +20,7 @@ constexpr int kThreads = 512;            // threads per CTA in every filter kern
 constexpr int kWarps = kThreads / 32;
 constexpr int kL1Bits = 11;              // first radix digit: 2048 buckets
 constexpr int kL1Bins = 1 << kL1Bits;
-constexpr double kMassScale = 1099511627776.0;  // 2^40 fixed-point units per unit of probability mass
-constexpr float kMassScaleF = 1099511627776.0f;
+constexpr float kMassScaleF = 1099511627776.0f;  // 2^40 fixed-point units per unit of probability mass
 
 
 // ------------------------------------------------------------------ dtypes
@@ -90,8 +90,81 @@ __device__ __forceinline__ float mass_f32(float v, const MassRef& r) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(t));
   return e;
 }
+// mass_f32 of two values at once: one packed (f32x2) fused multiply-add and
+// the same clamp and exponential per lane, so each lane equals mass_f32.
+__device__ __forceinline__ float2 mass2_f32(float2 v, const MassRef& r) {
+  unsigned long long xv, t;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(xv) : "f"(v.x), "f"(v.y));
+  const unsigned long long s2 = 0x3fb8aa3b3fb8aa3bull;  // 1.4426950408889634f in both lanes
+  unsigned long long b2;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(b2) : "f"(r.neg_m_log2e));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(t) : "l"(xv), "l"(s2), "l"(b2));
+  float t0, t1, e0, e1;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(t0), "=f"(t1) : "l"(t));
+  t0 = fminf(t0, 0.0f);
+  t1 = fminf(t1, 0.0f);
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(t0));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(t1));
+  return make_float2(e0, e1);
+}
+// a + b lane by lane, one packed (f32x2) add
+__device__ __forceinline__ float2 add2_f32(float2 a, float2 b) {
+  unsigned long long x, y, z;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
+  float r0, r1;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(z));
+  return make_float2(r0, r1);
+}
+// A finite float >= 0 below 2^63 rounded to the nearest integer, ties to
+// even, in integer ALU operations.  (The library conversion to a 64-bit
+// integer runs on the FP64 pipe, which this GPU keeps very narrow.)
+__host__ __device__ __forceinline__ uint32_t float_bits(float f) {
+#ifdef __CUDA_ARCH__
+  return __float_as_uint(f);
+#else
+  uint32_t b;
+  memcpy(&b, &f, sizeof b);
+  return b;
+#endif
+}
+__host__ __device__ __forceinline__ unsigned long long f2ull_rn(float f) {
+  const uint32_t b = float_bits(f);
+  const uint32_t be = b >> 23;                  // biased exponent (sign is 0)
+  if (be == 0) return 0ull;                     // zero or subnormal (< 2^-126)
+  const uint32_t m = (b & 0x7fffffu) | 0x800000u;
+  const int e = (int)be - 150;                  // f = m * 2^e
+  if (e >= 0) return (unsigned long long)m << e;
+  const int k = -e;
+  if (k > 24) return 0ull;                      // m / 2^k < 1/2
+  const uint32_t q = m >> k;
+  const uint32_t rem = m & ((1u << k) - 1u);
+  const uint32_t half = 1u << (k - 1);
+  return (unsigned long long)(q + ((rem > half || (rem == half && (q & 1u))) ? 1u : 0u));
+}
 __device__ __forceinline__ unsigned long long mass_fixed(float v, const MassRef& r) {
-  return __float2ull_rn(mass_f32(v, r) * kMassScaleF);
+  return f2ull_rn(mass_f32(v, r) * kMassScaleF);
+}
+
+// floor(thr * S) for thr in [0, 1], exactly, in integer operations: masked
+// iff the cumulative mass is <= thr * S.
+__host__ __device__ __forceinline__ unsigned long long mass_target(float thr, unsigned long long S) {
+  if (!(thr > 0.0f)) return 0ull;
+  if (thr >= 1.0f) return S;
+  const uint32_t b = float_bits(thr);
+  const uint32_t be = b >> 23;
+  const uint32_t m = be ? ((b & 0x7fffffu) | 0x800000u) : (b & 0x7fffffu);
+  const int sh = 150 - (int)(be ? be : 1u);     // thr = m * 2^-sh, sh >= 24
+  const unsigned long long lo = S * (unsigned long long)m;
+#ifdef __CUDA_ARCH__
+  const unsigned long long hi = __umul64hi(S, (unsigned long long)m);
+#else
+  const unsigned long long hi = (unsigned long long)(((unsigned __int128)S * m) >> 64);
+#endif
+  if (sh >= 128) return 0ull;
+  if (sh >= 64) return hi >> (sh - 64);
+  return (lo >> sh) | (hi << (64 - sh));
 }
 
 // round_D(1 - p): ``1 - p`` on a p tensor of the logits dtype
@@ -294,6 +367,54 @@ __device__ __forceinline__ unsigned long long block_exclusive_scan(unsigned long
   *total = ws[kWarps - 1];
   __syncthreads();
   return base + x - v;
+}
+
+// Two exclusive prefix sums at once (one set of barriers): *ea / *eb get
+// the prefixes of a / b, *ta / *tb their totals.  `ws` is 2 * kWarps words
+// of shared scratch.  Contains __syncthreads().
+__device__ __forceinline__ void block_exclusive_scan2(unsigned long long a, unsigned long long b,
+                                                      unsigned long long* ea, unsigned long long* eb,
+                                                      unsigned long long* ta, unsigned long long* tb,
+                                                      unsigned long long* ws) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long x = a, y = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long xu = __shfl_up_sync(0xffffffffu, x, o);
+    const unsigned long long yu = __shfl_up_sync(0xffffffffu, y, o);
+    if (lane >= o) {
+      x += xu;
+      y += yu;
+    }
+  }
+  if (lane == 31) {
+    ws[warp] = x;
+    ws[kWarps + warp] = y;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long u = lane < kWarps ? ws[lane] : 0ull;
+    unsigned long long w = lane < kWarps ? ws[kWarps + lane] : 0ull;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long uu = __shfl_up_sync(0xffffffffu, u, o);
+      const unsigned long long wu = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) {
+        u += uu;
+        w += wu;
+      }
+    }
+    if (lane < kWarps) {
+      ws[lane] = u;
+      ws[kWarps + lane] = w;
+    }
+  }
+  __syncthreads();
+  *ea = (warp ? ws[warp - 1] : 0ull) + x - a;
+  *eb = (warp ? ws[kWarps + warp - 1] : 0ull) + y - b;
+  *ta = ws[kWarps - 1];
+  *tb = ws[2 * kWarps - 1];
+  __syncthreads();
 }
 
 __device__ __forceinline__ unsigned long long block_sum(unsigned long long v, unsigned long long* ws) {

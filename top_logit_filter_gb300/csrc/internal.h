@@ -27,12 +27,15 @@ struct ApplyArgs {
 constexpr int32_t kApplyForceGeneric = 1;
 
 // Shared memory of one apply CTA: header (small histograms, scan scratch),
-// a 4096-bin histogram, and a 64 KB region for the per-warp candidate lists
-// (or per-warp window counts, or generic-path mass bins).
+// a 4096-entry table (bucket histogram, or bucket -> count block), a 10 KB
+// auxiliary region (count block -> bucket, block masses), and a 64 KB region
+// for the per-key count blocks (or the per-warp candidate lists, or the
+// generic path's mass bins).
 constexpr size_t kApplyHdrBytes = 4096;
 constexpr size_t kApplyHistBytes = 4096 * 4;
+constexpr size_t kApplyAuxBytes = 1024 * 2 + 1024 * 8;
 constexpr size_t kApplyBigBytes = 65536;
-constexpr size_t kApplySmem = kApplyHdrBytes + kApplyHistBytes + kApplyBigBytes;
+constexpr size_t kApplySmem = kApplyHdrBytes + kApplyHistBytes + kApplyAuxBytes + kApplyBigBytes;
 
 cudaError_t launch_apply(topkp_dtype dt, const ApplyArgs& a, cudaStream_t s);
 

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 2) sorted_kernel(const SortedArgs a)
       if (r < (int)crank) before += h.part[r];
       S += h.part[r];
     }
-    const unsigned long long target = (unsigned long long)floor((double)thr * (double)S);
+    const unsigned long long target = mass_target(thr, S);
     // the rank whose part holds the first cumulative mass above target
     if (before <= target && target < before + part) {
       unsigned long long tot;
