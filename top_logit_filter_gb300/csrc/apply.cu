@@ -63,6 +63,7 @@ constexpr int kKeyBlocks = (int)(kApplyBigBytes / (16 * 4));  // 16-key count bl
 static_assert(kApplyAuxBytes >= (size_t)kKeyBlocks * (2 + 8), "block -> bucket map and block masses");
 static_assert(2 * kBins * 8 <= (int)kApplyBigBytes, "bucket mass bounds fit the big region");
 constexpr uint32_t kNoBlock = 0xffffffffu;   // bucket without a count block
+constexpr int kMassBins = (int)(kApplyBigBytes / 4);  // per-key counters of the bf16 mass-table path
 constexpr int kLoadsSimple = 8;              // vectors in flight per lane, light per-vector work
 constexpr int kLoadsHeavy = 4;               // vectors in flight per lane, per-element work
 
@@ -77,6 +78,7 @@ struct __align__(16) ApplyHdr {
   uint32_t maxkey;                      // row max key
   uint32_t over;                        // a candidate list overflowed
   int w0, w1;                           // window path: first / last bucket of the window
+  uint32_t k_lo, z_lo, z_hi, nbins;     // mass-table path: first key, zero-mass-equal keys, bins
 };
 static_assert(sizeof(ApplyHdr) <= kApplyHdrBytes, "header too large");
 
@@ -284,6 +286,73 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
 }
 
 
+
+// Smallest key in [lo, hi] where a predicate that is false then true over
+// the keys holds (pred(hi) must hold), searched by the whole CTA: every
+// round tests one evenly spaced key per thread.  `slot` is shared scratch.
+template <typename Pred>
+__device__ __forceinline__ uint32_t block_first_true(uint32_t lo, uint32_t hi, Pred pred, uint32_t* slot) {
+  while (true) {
+    const uint32_t span = hi - lo + 1;
+    const uint32_t stride = (span + kThreads - 1) / kThreads;
+    if (threadIdx.x == 0) *slot = hi;
+    __syncthreads();
+    const uint32_t key = lo + threadIdx.x * stride;
+    if (key < hi && pred(key)) atomicMin(slot, key);
+    __syncthreads();
+    const uint32_t first = *slot;
+    __syncthreads();
+    if (stride == 1) return first;
+    lo = first >= lo + stride - 1 ? first - (stride - 1) : lo;
+    hi = first;
+  }
+}
+
+// The top-p cut over n bins in ascending key order: bin i holds cnt(i)
+// elements of key key_of(i), each of mass mass_fixed(value(key_of(i))).
+// Bins below `first` are left out (top-k masked them).  Bins are spread
+// evenly over the threads; one block scan gives the mass S and the target
+// floor(thr * S), and the thread owning the bin where the ascending
+// cumulative mass passes the target resolves the key and the masked ties.
+// last: the target reaches S (only the last sorted position survives).
+// Otherwise .bin is the cut key and .off the masked ties, or .bin = -1 when
+// the cut falls in a bin that ok(i) rejects.
+template <int DT, typename Cnt, typename KeyOf, typename Ok>
+__device__ __forceinline__ Sel mass_cut(int n, int first, Cnt cnt, KeyOf key_of, Ok ok, const MassRef& mr, float thr,
+                                        ApplyHdr& h, bool* last) {
+  const int bpt = (n + kThreads - 1) / kThreads;
+  const int b0 = min(n, (int)threadIdx.x * bpt), b1 = min(n, b0 + bpt);
+  unsigned long long s = 0;
+#pragma unroll 4
+  for (int i = max(b0, first); i < b1; ++i) {
+    const uint32_t c = cnt(i);
+    if (c) s += (unsigned long long)c * mass_fixed(value_of_key<DT>(key_of(i)), mr);
+  }
+  unsigned long long S;
+  const unsigned long long ex = block_exclusive_scan(s, &S, h.ws);
+  const unsigned long long target = mass_target(thr, S);
+  *last = target >= S;
+  if (*last) return Sel{-1, 0ull};
+  if (ex <= target && target < ex + s) {
+    unsigned long long acc = ex;
+    for (int i = max(b0, first); i < b1; ++i) {
+      const uint32_t c = cnt(i);
+      if (!c) continue;
+      const unsigned long long u = mass_fixed(value_of_key<DT>(key_of(i)), mr);
+      const unsigned long long mk = (unsigned long long)c * u;
+      if (target < acc + mk) {
+        if (ok(i)) {
+          h.sel_bin = (int)key_of(i);
+          h.sel_off = u ? (target - acc) / u : 0ull;
+        }
+        break;
+      }
+      acc += mk;
+    }
+  }
+  return finish_select(h);
+}
+
 enum TieRule : int { kTiesKept = 0, kTiesMasked = 1, kTiesStraddle = 2, kKeepAll = 3 };
 
 template <int DT>
@@ -442,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         atomicAdd(&hist[key >> SHB], 1u);
       }
     });
-  } else if (window) {
+  } else if (window && DT != TOPKP_BF16) {
     if constexpr (KB == 16) {
       sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
         if (nv) kmax = max(kmax, vmax_key(q));
@@ -517,20 +586,16 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
           const int bk = select_desc_f<BPT>(cnt, (unsigned long long)kv, h).bin;
           T = Lkey + (uint32_t)bk;
           if (topp) {
-            auto mb = [&](int j) -> unsigned long long {
-              const int bin = BPT * tid + j;
-              return (bin >= bk && hist[bin]) ? hist[bin] * mass_fixed(value_of_key<DT>(Lkey + bin), mr) : 0ull;
-            };
-            const unsigned long long S = block_sum_f<BPT>(mb, h.ws);
-            const unsigned long long target = mass_target(thr, S);
-            const Sel sp = select_asc_f<BPT>(mb, target, h);
-            if (sp.bin < 0) {
+            bool last;
+            const Sel sp = mass_cut<DT>(
+                (int)(gmax - Lkey) + 1, bk, [&](int i) { return hist[i]; },
+                [&](int i) { return Lkey + (uint32_t)i; }, [](int) { return true; }, mr, thr, h, &last);
+            if (last) {
               cut_last = true;
               r0 = hist[gmax - Lkey] - 1ull;
             } else {
-              T = Lkey + (uint32_t)sp.bin;
-              const unsigned long long u = mass_fixed(value_of_key<DT>(T), mr);
-              r0 = u ? (target - sp.off) / u : 0ull;
+              T = (uint32_t)sp.bin;
+              r0 = sp.off;
             }
           }
         } else {
@@ -606,8 +671,104 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     }
   }
 
+  // ------------------------------------------------------ mass-table path
+  // bf16 rows with top-p only.  With 128 keys per binade, the keys whose
+  // fixed-point mass is non-zero (value > max - 28.4) number a few thousand
+  // once the keys around zero whose fp32 mass equals that of zero share one
+  // bin.  One pass of per-key counts then gives the row mass, every
+  // cumulative mass and the cut exactly; elements of zero mass are always
+  // masked and never counted.  Rows whose range does not fit, or whose cut
+  // falls among the zero-equal keys, take the window path.
+  bool window_counted = DT != TOPKP_BF16;  // the window path's bucket counts exist
+  if (window && DT == TOPKP_BF16) {
+    uint32_t* tab = kcount;
+    {
+      // mass_f32 is non-decreasing in the key, so block-wide searches find
+      // the first key of non-zero fixed-point mass and the zero-equal keys
+      auto mfix = [&](uint32_t key) { return mass_fixed(value_of_key<DT>(key), mr); };
+      auto mf = [&](uint32_t key) { return mass_f32(value_of_key<DT>(key), mr); };
+      constexpr uint32_t H = 1u << (KB - 1);  // key of zero
+      // keys at or below that of -inf are -inf and negative NaN patterns
+      const uint32_t kfin = order_key<DT>(D::kNegInf) + 1u;
+      const uint32_t klo = block_first_true(kfin, gmax, [&](uint32_t key) { return mfix(key) > 0; }, &h.k_lo);
+      uint32_t zlo = 0x10000u, zhi = 0x10000u;  // no shared bin
+      if (klo <= H && H <= gmax) {
+        const float f0 = mf(H);
+        zhi = block_first_true(H, gmax + 1, [&](uint32_t key) { return key > gmax || mf(key) != f0; }, &h.z_hi) - 1;
+        zlo = block_first_true(klo, H, [&](uint32_t key) { return mf(key) == f0; }, &h.z_lo);
+      }
+      if (tid == 0) {
+        h.k_lo = klo;
+        h.z_lo = zlo;
+        h.z_hi = zhi;
+        h.nbins = (zlo <= gmax) ? (zlo - klo) + 1 + (gmax - zhi) : gmax - klo + 1;
+      }
+      __syncthreads();
+    }
+    const uint32_t klo = h.k_lo, zlo = h.z_lo, zhi = h.z_hi, nbins = h.nbins;
+    if (nbins <= (uint32_t)kMassBins) {
+      for (int i = tid; i < (int)(nbins + 3) / 4; i += kThreads) reinterpret_cast<uint4*>(tab)[i] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+      // pass B (from L2): per-key counts; bin = key - klo, with the keys
+      // zlo..zhi folded onto one bin
+      const uint32_t zspan = zhi - zlo;
+      sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int) {
+        if constexpr (KB == 16) {
+          const uint32_t kp[4] = {order_keys2(q.x), order_keys2(q.y), order_keys2(q.z), order_keys2(q.w)};
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) {
+            const uint32_t key = (j & 1) ? (kp[j >> 1] >> 16) : (kp[j >> 1] & 0xffffu);
+            if (key >= klo) {  // the -inf padding never is
+              const uint32_t fold = min(max(key, zlo) - zlo, zspan);
+              atomicAdd(&tab[key - klo - fold], 1u);
+            }
+          }
+        }
+      });
+      __syncthreads();
+      // bin i holds key klo + i below the shared bin, key zhi + (i - nlow)
+      // above it; the shared bin has the mass of zero
+      const uint32_t nlow = zlo <= gmax ? zlo - klo : nbins;
+      auto key_of = [&](int i) -> uint32_t {
+        return (uint32_t)i < nlow ? klo + (uint32_t)i
+                                  : ((uint32_t)i == nlow ? (1u << (KB - 1)) : zhi + ((uint32_t)i - nlow));
+      };
+      bool last;
+      const Sel sp = mass_cut<DT>(
+          (int)nbins, 0, [&](int i) { return tab[i]; }, key_of,
+          [&](int i) { return (uint32_t)i != nlow || zlo == zhi; },  // a shared bin of several keys has no cut key
+          mr, thr, h, &last);
+      if (last) {
+        cut_last = true;
+        T = gmax;
+        r0_known = false;
+        done = true;
+      } else if (sp.bin >= 0) {
+        T = (uint32_t)sp.bin;
+        r0 = sp.off;
+        done = true;
+      }
+    }
+    if (!done) {
+      // fall back to the window path: it needs the bucket counts
+      __syncthreads();
+      if constexpr (KB == 16) {
+        sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
+          const uint32_t kp[4] = {order_keys2(q.x), order_keys2(q.y), order_keys2(q.z), order_keys2(q.w)};
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) {
+            const uint32_t key = (j & 1) ? (kp[j >> 1] >> 16) : (kp[j >> 1] & 0xffffu);
+            if (j < nv) atomicAdd(&hist[key >> SHB], 1u);
+          }
+        });
+      }
+      __syncthreads();
+      window_counted = true;
+    }
+  }
+
   // ------------------------------------------------------- window path
-  if (window) {
+  if (window && !done && window_counted) {
     constexpr int BPT = kBins / kThreads;  // thread t owns buckets BPT*t .. BPT*t+BPT-1
     unsigned long long* lo_m = reinterpret_cast<unsigned long long*>(big);  // [kBins]
     unsigned long long* hi_m = lo_m + kBins;                                // [kBins]
