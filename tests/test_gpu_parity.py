@@ -40,6 +40,18 @@ def _rows(rng, B, V, dtype, kind):
         lo, hi = (-20.0, 14.0) if dtype == "f16" else (-60.0, 60.0)
         sign = np.where(rng.random((B, V)) < 0.5, -1.0, 1.0)
         x = (sign * np.exp2(rng.uniform(lo, hi, size=(B, V)))).astype(np.float32)
+    elif kind == "logprob":
+        # every value negative (log-probabilities)
+        x = (-np.abs(rng.standard_normal((B, V))) * 3 - 0.01).astype(np.float32)
+    elif kind == "shifted":
+        # every value far above zero: no negative value carries mass
+        x = (rng.standard_normal((B, V)) * 2 + 40).astype(np.float32)
+    elif kind == "late_max":
+        # negative rows whose maximum sits in the last percent of the row,
+        # after the first load group of every warp
+        x = (-np.abs(rng.standard_normal((B, V))) * 3 - 1).astype(np.float32)
+        for b in range(B):
+            x[b, V - 1 - int(rng.integers(0, max(1, V // 100)))] = 2.5 + b
     else:  # "zeros": signed zeros and a few values
         x = rng.choice(np.array([-0.0, 0.0, 1.0, -1.0, 2.0], dtype=np.float32), size=(B, V))
     return np.stack([to_raw(r, dtype) for r in x])
@@ -81,7 +93,7 @@ PLANS = ["", "generic"]
 def test_small_rows_all_plans(tk, monkeypatch, dtype, V, mode):
     rng = np.random.default_rng(V * 7 + len(mode))
     B = 9
-    for kind in ("normal", "ties", "zeros", "wide"):
+    for kind in ("normal", "ties", "zeros", "wide", "logprob", "shifted"):
         x = _rows(rng, B, V, dtype, kind)
         k, p = _kp(rng, B, V, dtype, mode)
         for plan in PLANS:
@@ -96,7 +108,7 @@ def test_multi_slice_rows(tk, monkeypatch, dtype):
     partial last warp step and a tail shorter than 16 bytes."""
     rng = np.random.default_rng(3)
     B, V = 6, 40011
-    for kind in ("normal", "ties", "wide"):
+    for kind in ("normal", "ties", "wide", "logprob", "shifted", "late_max"):
         x = _rows(rng, B, V, dtype, kind)
         k, p = _kp(rng, B, V, dtype, "kp")
         k[:3] = [0, 37, 900]
@@ -104,6 +116,9 @@ def test_multi_slice_rows(tk, monkeypatch, dtype):
             monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
             out = _run_apply(tk, x, dtype, p, k)
             _check_all(out, x, dtype, p, k, f"{dtype} {kind} plan={plan!r}")
+            # top-p only (k absent): the mass-table and window paths
+            out = _run_apply(tk, x, dtype, p, None)
+            _check_all(out, x, dtype, p, None, f"{dtype} {kind} top-p only plan={plan!r}")
 
 
 @pytest.mark.parametrize("dtype", DTS)

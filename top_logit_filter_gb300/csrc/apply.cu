@@ -78,7 +78,9 @@ struct __align__(16) ApplyHdr {
   uint32_t maxkey;                      // row max key
   uint32_t over;                        // a candidate list overflowed
   int w0, w1;                           // window path: first / last bucket of the window
-  uint32_t k_lo, z_lo, z_hi, nbins;     // mass-table path: first key, zero-mass-equal keys, bins
+  uint32_t mt_a, mt_b, mt_floor, mt_k0;  // mass-table path: bin = a - mag (x < 0) or b + mag (x >= 0),
+  int mt_qn;                             // mag clamped to >= floor; qn = bin of the negative floor;
+  uint32_t mt_lump;                      // k0 = provisional max key; lump: floors hold zero-equal keys
 };
 static_assert(sizeof(ApplyHdr) <= kApplyHdrBytes, "header too large");
 
@@ -400,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   const bool topp = a.p != nullptr;
   const bool keepall = !topk && !topp;
   const bool window = !topk && topp && KB == 16 && !generic_only;
+  const bool masstab = window && DT == TOPKP_BF16;
   const bool in_place = reinterpret_cast<const void*>(xr) == reinterpret_cast<const void*>(orow);
   if (keepall && in_place) return;  // nothing to filter, nothing to move
 
@@ -427,6 +430,8 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   if (tid < kWarps) h.nseg[tid] = 0;
   if ((topk && !generic_only) || window)
     for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+  if (masstab)
+    for (int i = tid; i < kMassBins / 4; i += kThreads) reinterpret_cast<uint4*>(kcount)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
 
   // n elements from row offset e0 as a vector, the rest -inf
@@ -479,6 +484,42 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       f(e0, q, lane == 0 ? tail : 0);
     }
   };
+  // sweep() whose first load group (and the head / tail vectors) is read
+  // before anything is processed; pre(q, head_vector, tail_vector) then runs
+  // in every thread (it may synchronise the CTA), and f sees the row as in
+  // sweep().
+  auto sweep_pre = [&](auto U_c, auto&& pre, auto&& f) {
+    constexpr int U = decltype(U_c)::value;
+    uint4 q[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = wb + u * 32 + lane;
+      q[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
+      if (v < we) q[u] = __ldcg(xv + v);
+    }
+    const uint4 hq = load_partial(0, (warp == 0 && lane == 0) ? head : 0);
+    const uint4 tq = load_partial(head + nvec * VEC, (warp == kWarps - 1 && lane == 0) ? tail : 0);
+    pre(q, hq, tq);
+    if (warp == 0 && head > 0) f(0, hq, lane == 0 ? head : 0);
+    for (int s0 = 0; s0 < nsteps; s0 += U) {
+      if (s0 > 0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = wb + (s0 + u) * 32 + lane;
+          q[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
+          if (v < we) q[u] = __ldcg(xv + v);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (s0 + u < nsteps) {
+          const int v = wb + (s0 + u) * 32 + lane;
+          f(head + v * VEC, q[u], v < we ? VEC : 0);
+        }
+      }
+    }
+    if (warp == kWarps - 1 && tail > 0) f(head + nvec * VEC, tq, lane == 0 ? tail : 0);
+  };
   auto each_elem = [&](auto&& g) {
     sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
 #pragma unroll
@@ -511,6 +552,80 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         atomicAdd(&hist[key >> SHB], 1u);
       }
     });
+  } else if (masstab) {
+    // A provisional max m0 (of every warp's first load group) fixes a table
+    // in ascending key order that holds every key of non-zero mass for any
+    // row max m >= m0.  It starts below m0 - 29.5 (mass 0 there for every m >=
+    // m0).  A bf16 value of magnitude `mag` lands in bin a - mag (x < 0) or
+    // b + mag (x >= 0) with mag first raised to a floor: when the range
+    // crosses zero, magnitudes below 2^(e - 26) (e = exponent of m0 log2 e)
+    // share the two floor bins -- for every m >= m0 > 0 the fused
+    // multiply-add of mass_f32 rounds such x away, so their fp32 mass is
+    // that of zero; otherwise the floor is the magnitude of m0 or of the
+    // range's first key.  Bins outside the table (zero-mass negatives) are
+    // skipped; a true max that needs a bin past the table, or values above
+    // m0 merged by the floor, send the row to the window path.
+    if constexpr (KB == 16) {
+      uint32_t ta = 0, tb = 0, tfloor = 0;
+      sweep_pre(
+          Loads<kLoadsHeavy>{},
+          [&](const uint4 (&q)[kLoadsHeavy], const uint4& hq, const uint4& tq) {
+            uint32_t km = max(vmax_key(hq), vmax_key(tq));
+#pragma unroll
+            for (int u = 0; u < kLoadsHeavy; ++u) km = max(km, vmax_key(q[u]));
+            km = __reduce_max_sync(0xffffffffu, km);
+            if (lane == 0) atomicMax(&h.maxkey, km);
+            __syncthreads();
+            const uint32_t k0 = h.maxkey;
+            const float m0 = value_of_key<DT>(k0);
+            constexpr uint32_t H = 1u << (KB - 1);
+            const uint32_t kfin = order_key<DT>(D::kNegInf) + 1u;
+            // first key: the bf16 at or below m0 - 29.5, one key lower still
+            const uint32_t vb = __float_as_uint(m0 - 29.5f);
+            const uint32_t r16 = (vb >> 16) + ((vb & 0x80000000u) && (vb & 0xffffu) ? 1u : 0u);
+            const uint32_t klo = max(kfin, order_key<DT>((raw)r16) - 1u);
+            uint32_t lump = 0, qn;
+            if (klo < H) {
+              const uint32_t mag_lo = H - klo;
+              if (m0 > 0.0f) {
+                const int e = (int)((__float_as_uint(m0 * 1.4426950408889634f) >> 23) & 0xffu) - 127 - 26;
+                tfloor = e + 127 > 0 ? ((uint32_t)(e + 127) << 7) - 1u : 0u;  // largest magnitude below 2^e
+                lump = 1;
+              } else {
+                tfloor = H - k0;  // magnitude of m0 (0 for m0 = 0)
+              }
+              ta = mag_lo;
+              qn = mag_lo - tfloor;
+            } else {
+              tfloor = klo - H;  // positives only; the floor bin has zero mass
+              ta = 0;            // every negative falls outside the table
+              qn = 0xffffffffu;
+            }
+            // positives from the shared floor bin up (the negative floor bin when
+            // the range crosses zero, else bin 0): both signs of a magnitude
+            // at or below the floor -- and so -0 and +0 -- share one bin
+            tb = (klo < H ? qn : 0u) - tfloor;
+            if (tid == 0) {
+              h.mt_a = ta;
+              h.mt_b = tb;
+              h.mt_floor = tfloor;
+              h.mt_k0 = k0;
+              h.mt_qn = (int)qn;
+              h.mt_lump = lump;
+            }
+          },
+          [&](int, const uint4& q, int nv) {
+            if (nv) kmax = max(kmax, vmax_key(q));
+            const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+              const uint32_t v = (j & 1) ? (wd[j >> 1] >> 16) : (wd[j >> 1] & 0xffffu);
+              const uint32_t mc = max(v & 0x7fffu, tfloor);
+              const uint32_t bin = (v & 0x8000u) ? ta - mc : tb + mc;
+              if (bin < (uint32_t)kMassBins) atomicAdd(&kcount[bin], 1u);  // never the -inf padding
+            }
+          });
+    }
   } else if (window && DT != TOPKP_BF16) {
     if constexpr (KB == 16) {
       sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
@@ -679,65 +794,30 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   // cumulative mass and the cut exactly; elements of zero mass are always
   // masked and never counted.  Rows whose range does not fit, or whose cut
   // falls among the zero-equal keys, take the window path.
-  bool window_counted = DT != TOPKP_BF16;  // the window path's bucket counts exist
-  if (window && DT == TOPKP_BF16) {
+  bool window_counted = !masstab;  // the window path's bucket counts exist
+  if (masstab) {
     uint32_t* tab = kcount;
-    {
-      // mass_f32 is non-decreasing in the key, so block-wide searches find
-      // the first key of non-zero fixed-point mass and the zero-equal keys
-      auto mfix = [&](uint32_t key) { return mass_fixed(value_of_key<DT>(key), mr); };
-      auto mf = [&](uint32_t key) { return mass_f32(value_of_key<DT>(key), mr); };
-      constexpr uint32_t H = 1u << (KB - 1);  // key of zero
-      // keys at or below that of -inf are -inf and negative NaN patterns
-      const uint32_t kfin = order_key<DT>(D::kNegInf) + 1u;
-      const uint32_t klo = block_first_true(kfin, gmax, [&](uint32_t key) { return mfix(key) > 0; }, &h.k_lo);
-      uint32_t zlo = 0x10000u, zhi = 0x10000u;  // no shared bin
-      if (klo <= H && H <= gmax) {
-        const float f0 = mf(H);
-        zhi = block_first_true(H, gmax + 1, [&](uint32_t key) { return key > gmax || mf(key) != f0; }, &h.z_hi) - 1;
-        zlo = block_first_true(klo, H, [&](uint32_t key) { return mf(key) == f0; }, &h.z_lo);
-      }
-      if (tid == 0) {
-        h.k_lo = klo;
-        h.z_lo = zlo;
-        h.z_hi = zhi;
-        h.nbins = (zlo <= gmax) ? (zlo - klo) + 1 + (gmax - zhi) : gmax - klo + 1;
-      }
-      __syncthreads();
-    }
-    const uint32_t klo = h.k_lo, zlo = h.z_lo, zhi = h.z_hi, nbins = h.nbins;
-    if (nbins <= (uint32_t)kMassBins) {
-      for (int i = tid; i < (int)(nbins + 3) / 4; i += kThreads) reinterpret_cast<uint4*>(tab)[i] = make_uint4(0, 0, 0, 0);
-      __syncthreads();
-      // pass B (from L2): per-key counts; bin = key - klo, with the keys
-      // zlo..zhi folded onto one bin
-      const uint32_t zspan = zhi - zlo;
-      sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int) {
-        if constexpr (KB == 16) {
-          const uint32_t kp[4] = {order_keys2(q.x), order_keys2(q.y), order_keys2(q.z), order_keys2(q.w)};
-#pragma unroll
-          for (int j = 0; j < VEC; ++j) {
-            const uint32_t key = (j & 1) ? (kp[j >> 1] >> 16) : (kp[j >> 1] & 0xffffu);
-            if (key >= klo) {  // the -inf padding never is
-              const uint32_t fold = min(max(key, zlo) - zlo, zspan);
-              atomicAdd(&tab[key - klo - fold], 1u);
-            }
-          }
-        }
-      });
-      __syncthreads();
-      // bin i holds key klo + i below the shared bin, key zhi + (i - nlow)
-      // above it; the shared bin has the mass of zero
-      const uint32_t nlow = zlo <= gmax ? zlo - klo : nbins;
-      auto key_of = [&](int i) -> uint32_t {
-        return (uint32_t)i < nlow ? klo + (uint32_t)i
-                                  : ((uint32_t)i == nlow ? (1u << (KB - 1)) : zhi + ((uint32_t)i - nlow));
+    const uint32_t ta = h.mt_a, tb = h.mt_b, tfloor = h.mt_floor, k0 = h.mt_k0, lump = h.mt_lump;
+    const int qn = h.mt_qn;
+    constexpr uint32_t H = 1u << (KB - 1);
+    // bin of the true max: past the table, or values above m0 merged into a
+    // floor bin without the zero-equal guarantee, send the row to the window path
+    const uint32_t graw = (uint32_t)raw_of_key<DT>(gmax);
+    const uint32_t gbin = (graw & 0x8000u) ? ta - max(graw & 0x7fffu, tfloor) : tb + max(graw & 0x7fffu, tfloor);
+    if (gbin < (uint32_t)kMassBins && (lump || qn < 0 || gmax == k0)) {
+      // bin v holds key H - (a - v) up to the floor bin qn, key
+      // H + (v - pbase + floor) above it (pbase: the floor bin, 0 when no
+      // negative carries mass); a floor bin of several keys carries the mass
+      // of zero and cannot hold the cut
+      const int pbase = qn >= 0 ? qn : 0;
+      auto key_of = [&](int v) -> uint32_t {
+        return v <= qn ? H - (ta - (uint32_t)v) : H + ((uint32_t)(v - pbase) + tfloor);
       };
+      const bool shared_floor = lump && tfloor > 0;
       bool last;
       const Sel sp = mass_cut<DT>(
-          (int)nbins, 0, [&](int i) { return tab[i]; }, key_of,
-          [&](int i) { return (uint32_t)i != nlow || zlo == zhi; },  // a shared bin of several keys has no cut key
-          mr, thr, h, &last);
+          (int)gbin + 1, 0, [&](int v) { return tab[v]; }, key_of,
+          [&](int v) { return !(shared_floor && v == qn); }, mr, thr, h, &last);
       if (last) {
         cut_last = true;
         T = gmax;
