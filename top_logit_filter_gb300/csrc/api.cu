@@ -79,10 +79,11 @@ SortedPlan plan_sorted(int64_t B, int64_t V, int esize, int num_sms, bool with_l
   int c = 0;
   if (force && *force) sscanf(force, "%d", &c);
   if (c <= 0) {
-    // about 48 KB of logits per CTA, at least two CTAs per SM overall
-    const int64_t bytes = V * esize;
-    c = (int)((bytes + 48 * 1024 - 1) / (48 * 1024));
-    if (c < 1) c = 1;
+    // one CTA per row; rows split over a cluster only when there are too
+    // few rows to give every SM two CTAs (the write of a row with few
+    // survivors is a fill plus a short scatter, so a CTA per row keeps the
+    // latency-bound boundary search to one per row)
+    c = 1;
     while (c < 8 && B * c < 2LL * num_sms && V / (c + 1) >= 2048) ++c;
   }
   if (c > 8) c = 8;

@@ -501,14 +501,14 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     const uint4 tq = load_partial(head + nvec * VEC, (warp == kWarps - 1 && lane == 0) ? tail : 0);
     pre(q, hq, tq);
     if (warp == 0 && head > 0) f(0, hq, lane == 0 ? head : 0);
+    // the next group's loads are in flight while this group is processed
     for (int s0 = 0; s0 < nsteps; s0 += U) {
-      if (s0 > 0) {
+      uint4 qn[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int v = wb + (s0 + u) * 32 + lane;
-          q[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
-          if (v < we) q[u] = __ldcg(xv + v);
-        }
+      for (int u = 0; u < U; ++u) {
+        const int v = wb + (s0 + U + u) * 32 + lane;
+        qn[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
+        if (v < we) qn[u] = __ldcg(xv + v);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -517,6 +517,8 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
           f(head + v * VEC, q[u], v < we ? VEC : 0);
         }
       }
+#pragma unroll
+      for (int u = 0; u < U; ++u) q[u] = qn[u];
     }
     if (warp == kWarps - 1 && tail > 0) f(head + nvec * VEC, tq, lane == 0 ? tail : 0);
   };

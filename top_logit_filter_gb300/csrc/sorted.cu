@@ -9,10 +9,15 @@
 //     point relative to the row maximum sorted[V-1]; J_p = first position
 //     whose ascending cumulative mass exceeds round_D(1-p) * S, else V-1;
 //   * everything at sorted positions >= J survives.
-// Output, with logits: out[v] = logits[v] if logits[v] > T, -inf if below,
-// and the elements tied with T = sorted[J] go through sorted_indices when the
-// tie group straddles J (the page's CompareSelectOnLogits + ScatterBoundary).
-// Without logits: out[sorted_indices[j]] = j >= J ? sorted[j] : -inf.
+// Output.  When the survivors (sorted positions J..V-1) are at most an
+// eighth of the row, the row is filled with -inf by coalesced vector stores
+// and only the survivors are scattered through sorted_indices: two bytes
+// per element plus the few survivors, and no tie handling, since the sorted
+// order already is the stable order.  Otherwise, with logits: out[v] =
+// logits[v] if logits[v] > T, -inf if below, and the elements tied with
+// T = sorted[J] go through sorted_indices when the tie group straddles J
+// (the page's CompareSelectOnLogits + ScatterBoundary); without logits:
+// out[sorted_indices[j]] = j >= J ? sorted[j] : -inf.
 //
 // Launch shape: one cluster of `csize` CTAs per row.  Each CTA owns one chunk
 // of the output and prefetches its logits chunk into shared memory with a
@@ -87,8 +92,14 @@ __global__ void __launch_bounds__(kThreads, 2) sorted_kernel(const SortedArgs a)
   const int c1 = (int)min((int64_t)c0 + a.chunk, (int64_t)V);
   const int n = c1 - c0;
 
-  // ---- prefetch this CTA's logits chunk (overlaps the boundary search) ----
-  const bool staged = lg != nullptr && a.aligned;
+  const int kv = a.k ? a.k[row] : 0;
+  const bool topk = a.k != nullptr && kv >= 1 && kv <= V - 1;
+  const bool topp = a.p != nullptr;
+
+  // ---- prefetch this CTA's logits chunk (overlaps the boundary search),
+  // unless top-k already promises few survivors (the logits go unread) ----
+  const bool few_expected = topk && kv <= V / 8;
+  const bool staged = lg != nullptr && a.aligned && !few_expected;
   const uint32_t bulk = staged ? ((uint32_t)n * (uint32_t)sizeof(raw)) & ~15u : 0u;
   if (tid == 0) {
     mbar_init(&h.mbar, 1);
@@ -100,10 +111,6 @@ __global__ void __launch_bounds__(kThreads, 2) sorted_kernel(const SortedArgs a)
     mbar_arrive_expect_tx(&h.mbar, bulk);
     bulk_g2s(stage, lg + c0, bulk, &h.mbar);
   }
-
-  const int kv = a.k ? a.k[row] : 0;
-  const bool topk = a.k != nullptr && kv >= 1 && kv <= V - 1;
-  const bool topp = a.p != nullptr;
 
   // ---- top-k boundary ([guide] §2 steps 1-3) ----
   int jk = 0;
@@ -165,7 +172,23 @@ __global__ void __launch_bounds__(kThreads, 2) sorted_kernel(const SortedArgs a)
   }
 
   // ---- write ([guide] §2 step 8) ----
-  if (lg != nullptr) {
+  if (V - J <= V / 8) {
+    // fill this CTA's chunk with -inf, then scatter the survivors
+    if (bulk && !mbar_wait_bounded(&h.mbar, 0, a.timeout_ns)) atomicOr(&g_device_error, 1u);
+    const uint32_t NEG2 = DType<DT>::kKeyBits == 16 ? ((uint32_t)D::kNegInf * 0x10001u) : (uint32_t)D::kNegInf;
+    raw* oc = o + c0;
+    const int head = ((uintptr_t)oc & 15u) ? min(n, (int)((16u - ((uintptr_t)oc & 15u)) / sizeof(raw))) : 0;
+    for (int i = tid; i < head; i += kThreads) oc[i] = D::kNegInf;
+    const int nv = (n - head) / VEC;
+    uint4* ov = reinterpret_cast<uint4*>(oc + head);
+    for (int i = tid; i < nv; i += kThreads) ov[i] = make_uint4(NEG2, NEG2, NEG2, NEG2);
+    for (int i = head + nv * VEC + tid; i < n; i += kThreads) oc[i] = D::kNegInf;
+    if (C > 1) cluster_sync_all(); else __syncthreads();
+    for (int j = J + (int)crank * kThreads + tid; j < V; j += C * kThreads) {
+      const int v = si[j];
+      if (v >= 0 && v < V) o[v] = sv[j];
+    }
+  } else if (lg != nullptr) {
     const float T = D::to_float(sv[J]);
     const bool any = topk || topp;
     const int lo_t = any ? lower_bound_back<DT>(sv, J, T) : J;
