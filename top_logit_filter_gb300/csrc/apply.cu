@@ -64,6 +64,7 @@ static_assert(kApplyAuxBytes >= (size_t)kKeyBlocks * (2 + 8), "block -> bucket m
 static_assert(2 * kBins * 8 <= (int)kApplyBigBytes, "bucket mass bounds fit the big region");
 constexpr uint32_t kNoBlock = 0xffffffffu;   // bucket without a count block
 constexpr int kMassBins = (int)(kApplyBigBytes / 4);  // per-key counters of the bf16 mass-table path
+constexpr int kTieRankMax = 1024;            // ties of the cut ranked by position for the scatter write
 constexpr int kLoadsSimple = 8;              // vectors in flight per lane, light per-vector work
 constexpr int kLoadsHeavy = 4;               // vectors in flight per lane, per-element work
 
@@ -77,6 +78,9 @@ struct __align__(16) ApplyHdr {
   int sel_bin;                          // select result: bin, -1 if none
   uint32_t maxkey;                      // row max key
   uint32_t over;                        // a candidate list overflowed
+  uint32_t fill;                        // write by a -inf fill plus a scatter of the listed survivors
+  uint32_t ntie;                        // ties of T gathered for ranking
+  uint32_t tie_cut;                     // position of the first kept tie of T
   int w0, w1;                           // window path: first / last bucket of the window
   uint32_t mt_a, mt_b, mt_floor, mt_k0;  // mass-table path: bin = a - mag (x < 0) or b + mag (x >= 0),
   int mt_qn;                             // mag clamped to >= floor; qn = bin of the negative floor;
@@ -374,7 +378,8 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   constexpr int KB = D::kKeyBits;
   constexpr int SHB = KB - 12;           // 12-bit first digit of the candidate / window paths
   constexpr int SH1 = L::shift(0);       // 11-bit first digit of the generic path
-  constexpr int CAPW = (int)(kApplyBigBytes / sizeof(ckey)) / kWarps;  // list entries per warp
+  // list entries per warp: the raw value and its position in the row
+  constexpr int CAPW = (int)(kApplyBigBytes / (sizeof(ckey) + 4)) / kWarps / 2 * 2;
 
   extern __shared__ __align__(128) unsigned char smem[];
   ApplyHdr& h = *reinterpret_cast<ApplyHdr*>(smem);
@@ -394,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   const raw* xr = reinterpret_cast<const raw*>(a.x) + row * a.ldx;
   raw* orow = reinterpret_cast<raw*>(a.out) + row * a.ldo;
   ckey* seg = reinterpret_cast<ckey*>(big) + warp * CAPW;
+  uint32_t* segi = reinterpret_cast<uint32_t*>(big + (size_t)kWarps * CAPW * sizeof(ckey)) + warp * CAPW;
   unsigned long long* mass = reinterpret_cast<unsigned long long*>(big);
 
   const bool generic_only = (a.force & kApplyForceGeneric) != 0;
@@ -423,6 +429,9 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   if (tid == 0) {
     h.maxkey = 0;
     h.over = 0;
+    h.fill = 0;
+    h.ntie = 0;
+    h.tie_cut = 0;
     h.sel_bin = -1;
     h.w0 = kBins - 1;
     h.w1 = kBins - 1;
@@ -667,14 +676,17 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       // pass B (from L2): every element >= L joins its warp's list
       const uint32_t Lkey = (uint32_t)lb << SHB;
       const uint32_t L2 = P::splat((uint32_t)raw_of_key<DT>(Lkey));
-      sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) {
+      sweep(Loads<kLoadsSimple>{}, false, [&](int e, const uint4& q, int nv) {
         if (nv != 0 && (P::ge(q.x, L2) | P::ge(q.y, L2) | P::ge(q.z, L2) | P::ge(q.w, L2)) != 0u) {
           uint32_t bits = ge_bits(q, nv, L2);
           uint32_t slot = atomicAdd(&h.nseg[warp], (uint32_t)__popc(bits));
           while (bits) {
             const int j = __ffs(bits) - 1;
             bits &= bits - 1;
-            if (slot < (uint32_t)CAPW) seg[slot] = (ckey)order_key<DT>(vec_elem<DT>(q, j));
+            if (slot < (uint32_t)CAPW) {
+              seg[slot] = (ckey)vec_elem<DT>(q, j);
+              segi[slot] = (uint32_t)(e + j);
+            }
             ++slot;
           }
         }
@@ -690,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         // ---- select on the lists (every element >= the k-th largest is listed) ----
         const int myn = (int)h.nseg[warp];
         auto each_own = [&](auto&& f) {
-          for (int j = lane; j < myn; j += 32) f((uint32_t)seg[j]);
+          for (int j = lane; j < myn; j += 32) f(order_key<DT>((raw)seg[j]));
         };
         if (KB == 16 && gmax - Lkey < (uint32_t)kBins) {
           // exact per-key counts over [L, max]: a 16-bit key is a value
@@ -779,11 +791,35 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         if (cut_last) T = gmax;
         done = true;
         // ties of T per warp, from the lists (T >= L is listed)
-        uint32_t ct = 0;
-        each_own([&](uint32_t key) { ct += (key == T); });
+        uint32_t ct = 0, cgt = 0;
+        each_own([&](uint32_t key) {
+          ct += (key == T);
+          cgt += (key > T);
+        });
         ct = __reduce_add_sync(0xffffffffu, ct);
         if (lane == 0) h.wtie[warp] = ct;
         have_wtie = true;
+        // The survivors are listed with their positions: when they are few,
+        // the write fills the row with -inf and scatters them, without a
+        // second read of the row.  Ties of T are ranked by position.
+        const unsigned long long ngt = block_sum(cgt, h.ws);
+        unsigned long long nties = 0;
+        for (int w = 0; w < kWarps; ++w) nties += h.wtie[w];
+        const bool fill = ngt + (nties - r0) <= (unsigned long long)(V / 8) && (r0 == 0 || nties <= kTieRankMax);
+        if (fill && r0 > 0) {
+          uint32_t* tpos = hist;  // free again: positions of the ties of T
+          for (int j = lane; j < myn; j += 32)
+            if (order_key<DT>((raw)seg[j]) == T) tpos[atomicAdd(&h.ntie, 1u)] = segi[j];
+          __syncthreads();
+          const int nt = (int)h.ntie;
+          for (int t = tid; t < nt; t += kThreads) {
+            const uint32_t mine = tpos[t];
+            int rank = 0;
+            for (int u = 0; u < nt; ++u) rank += tpos[u] < mine;
+            if (rank == (int)r0) h.tie_cut = mine;  // the first tie that stays
+          }
+        }
+        if (tid == 0) h.fill = fill ? 1u : 0u;
       }
     }
   }
@@ -1152,6 +1188,26 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     unsigned long long all = 0;
     for (int w = 0; w < kWarps; ++w) all += h.wtie[w];
     r0 = all - 1ull;
+  }
+
+  // ---- write: the listed survivors over a -inf row ([guide] §2 step 8) ----
+  if (h.fill) {
+    const uintptr_t oaddr = reinterpret_cast<uintptr_t>(orow);
+    const int ohead = min(V, (int)(((16u - (uint32_t)(oaddr & 15u)) & 15u) / (uint32_t)sizeof(raw)));
+    const int onv = (V - ohead) / VEC;
+    for (int i = tid; i < ohead; i += kThreads) orow[i] = D::kNegInf;
+    uint4* ov = reinterpret_cast<uint4*>(orow + ohead);
+    for (int i = tid; i < onv; i += kThreads) ov[i] = make_uint4(NEG2, NEG2, NEG2, NEG2);
+    for (int i = ohead + onv * VEC + tid; i < V; i += kThreads) orow[i] = D::kNegInf;
+    __syncthreads();
+    const int myn = (int)h.nseg[warp];
+    const uint32_t tcut = h.tie_cut;
+    for (int j = lane; j < myn; j += 32) {
+      const raw r = (raw)seg[j];
+      const uint32_t key = order_key<DT>(r);
+      if (key > T || (key == T && segi[j] >= tcut)) orow[segi[j]] = r;
+    }
+    return;
   }
 
   // ---- write pass: original element or -inf, in original order ([guide] §2 step 8) ----
