@@ -551,11 +551,59 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   // key of the largest element of a vector with at least one valid element
   auto vmax_key = [&](const uint4& q) -> uint32_t { return order_key<DT>((raw)P::max_raw(q)); };
 
+  // appends the elements of a vector that are >= the value filling the lanes
+  // of L2 to this warp's list, with their positions
+  auto append_ge = [&](int e, const uint4& q, int nv, uint32_t L2) {
+    if (nv != 0 && (P::ge(q.x, L2) | P::ge(q.y, L2) | P::ge(q.z, L2) | P::ge(q.w, L2)) != 0u) {
+      uint32_t bits = ge_bits(q, nv, L2);
+      uint32_t slot = atomicAdd(&h.nseg[warp], (uint32_t)__popc(bits));
+      while (bits) {
+        const int j = __ffs(bits) - 1;
+        bits &= bits - 1;
+        if (slot < (uint32_t)CAPW) {
+          seg[slot] = (ckey)vec_elem<DT>(q, j);
+          segi[slot] = (uint32_t)(e + j);
+        }
+        ++slot;
+      }
+    }
+  };
+  // Top-k with small k: the first load group of every warp bounds the
+  // candidates (k of its vectors reach the bucket floor of their k-th
+  // largest maximum), so pass A collects them and the row is read once,
+  // when the expected number of candidates fits the lists comfortably.
+  const int fv = min(nvec, kWarps * 32 * kLoadsHeavy);
+  const bool single = topk && !generic_only && kv <= fv &&
+                      4LL * kv * V <= (long long)fv * VEC * kWarps * CAPW;
+  uint32_t Lkey = 0;  // candidate bound (candidate path)
+
   // ---- pass A (from HBM): the row max, plus the 12-bit first-digit
   // histogram of the vector maxima (candidate path) or of every element
   // (window path) ----
   uint32_t kmax = 0;
-  if (topk && !generic_only) {
+  if (single) {
+    uint32_t L2 = 0;
+    sweep_pre(
+        Loads<kLoadsHeavy>{},
+        [&](const uint4 (&q)[kLoadsHeavy], const uint4& hq, const uint4& tq) {
+#pragma unroll
+          for (int u = 0; u < kLoadsHeavy; ++u)
+            if (wb + u * 32 + lane < we) atomicAdd(&hist[vmax_key(q[u]) >> SHB], 1u);
+          if (warp == 0 && lane == 0 && head > 0) atomicAdd(&hist[vmax_key(hq) >> SHB], 1u);
+          if (warp == kWarps - 1 && lane == 0 && tail > 0) atomicAdd(&hist[vmax_key(tq) >> SHB], 1u);
+          __syncthreads();
+          const int lb = select_desc_f<kBins / kThreads>(
+              [&](int j) -> unsigned long long { return hist[(kBins / kThreads) * tid + j]; },
+              (unsigned long long)kv, h).bin;
+          // fewer than k vectors in the groups: every element (the lists overflow)
+          Lkey = lb > 0 ? (uint32_t)lb << SHB : order_key<DT>(D::kNegInf) + 1u;
+          L2 = P::splat((uint32_t)raw_of_key<DT>(Lkey));
+        },
+        [&](int e, const uint4& q, int nv) {
+          if (nv) kmax = max(kmax, vmax_key(q));
+          append_ge(e, q, nv, L2);
+        });
+  } else if (topk && !generic_only) {
     sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) {
       if (nv) {
         const uint32_t key = vmax_key(q);
@@ -670,35 +718,47 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
 
   // ---------------------------------------------------- candidate path
   if (topk && !generic_only) {
-    const int lb = select_desc_f<kBins / kThreads>(
-        [&](int j) -> unsigned long long { return hist[(kBins / kThreads) * tid + j]; }, (unsigned long long)kv, h).bin;
-    if (lb > 0) {
-      // pass B (from L2): every element >= L joins its warp's list
-      const uint32_t Lkey = (uint32_t)lb << SHB;
-      const uint32_t L2 = P::splat((uint32_t)raw_of_key<DT>(Lkey));
-      sweep(Loads<kLoadsSimple>{}, false, [&](int e, const uint4& q, int nv) {
-        if (nv != 0 && (P::ge(q.x, L2) | P::ge(q.y, L2) | P::ge(q.z, L2) | P::ge(q.w, L2)) != 0u) {
-          uint32_t bits = ge_bits(q, nv, L2);
-          uint32_t slot = atomicAdd(&h.nseg[warp], (uint32_t)__popc(bits));
-          while (bits) {
-            const int j = __ffs(bits) - 1;
-            bits &= bits - 1;
-            if (slot < (uint32_t)CAPW) {
-              seg[slot] = (ckey)vec_elem<DT>(q, j);
-              segi[slot] = (uint32_t)(e + j);
-            }
-            ++slot;
-          }
-        }
-      });
-      __syncwarp();
+    bool listed = false;
+    if (single) {
       if (lane == 0 && h.nseg[warp] > (uint32_t)CAPW) {
         h.nseg[warp] = CAPW;
         h.over = 1;
       }
       __syncthreads();
-
-      if (!h.over) {
+      listed = !h.over;
+      if (!listed) {
+        // the bound from the first load groups was too loose: start over
+        // from the whole row's vector maxima
+        __syncthreads();
+        for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+        if (tid < kWarps) h.nseg[tid] = 0;
+        if (tid == 0) h.over = 0;
+        __syncthreads();
+        sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) {
+          if (nv) atomicAdd(&hist[vmax_key(q) >> SHB], 1u);
+        });
+        __syncthreads();
+      }
+    }
+    if (!listed) {
+      const int lb = select_desc_f<kBins / kThreads>(
+          [&](int j) -> unsigned long long { return hist[(kBins / kThreads) * tid + j]; }, (unsigned long long)kv, h).bin;
+      if (lb > 0) {
+        // pass B (from L2): every element >= L joins its warp's list
+        Lkey = (uint32_t)lb << SHB;
+        const uint32_t L2 = P::splat((uint32_t)raw_of_key<DT>(Lkey));
+        sweep(Loads<kLoadsSimple>{}, false, [&](int e, const uint4& q, int nv) { append_ge(e, q, nv, L2); });
+        __syncwarp();
+        if (lane == 0 && h.nseg[warp] > (uint32_t)CAPW) {
+          h.nseg[warp] = CAPW;
+          h.over = 1;
+        }
+        __syncthreads();
+        listed = !h.over;
+      }
+    }
+    {
+      if (listed) {
         // ---- select on the lists (every element >= the k-th largest is listed) ----
         const int myn = (int)h.nseg[warp];
         auto each_own = [&](auto&& f) {
