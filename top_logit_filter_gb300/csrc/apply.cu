@@ -1234,21 +1234,8 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     }
   }
 
-  // ---- ties of T per warp, where the path did not count them ----
   const uint32_t T2 = P::splat((uint32_t)raw_of_key<DT>(T));
-  if (!keepall && (r0 > 0 || !r0_known) && !have_wtie) {
-    uint32_t ct = 0;
-    sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) { ct += __popc(eq_bits(q, nv, T2)); });
-    ct = __reduce_add_sync(0xffffffffu, ct);
-    if (lane == 0) h.wtie[warp] = ct;
-  }
   __syncthreads();
-  if (!r0_known) {
-    // only the last sorted position survives: the last element equal to the max
-    unsigned long long all = 0;
-    for (int w = 0; w < kWarps; ++w) all += h.wtie[w];
-    r0 = all - 1ull;
-  }
 
   // ---- write: the listed survivors over a -inf row ([guide] §2 step 8) ----
   if (h.fill) {
@@ -1271,51 +1258,100 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   }
 
   // ---- write pass: original element or -inf, in original order ([guide] §2 step 8) ----
-  int rule = kKeepAll;
-  unsigned long long seen = 0;  // ties of T before this warp's next vector (straddling warp)
-  if (!keepall) {
-    if (r0 == 0) {
-      rule = kTiesKept;
-    } else {
-      unsigned long long pre = 0;
-      for (int w = 0; w < warp; ++w) pre += h.wtie[w];
-      const unsigned long long mine = h.wtie[warp];
-      rule = (pre + mine <= r0) ? kTiesMasked : (pre >= r0 ? kTiesKept : kTiesStraddle);
-      seen = pre;
-    }
-  }
-  sweep(Loads<kLoadsSimple>{}, true, [&](int e, const uint4& qin, int nv) {
-    uint32_t keep_ties = 0;  // rule == kTiesStraddle: ties of this vector that stay
-    if (rule == kTiesStraddle) {
-      uint32_t tb = eq_bits(qin, nv, T2);
-      const uint32_t cnt = __popc(tb);
-      if (__any_sync(0xffffffffu, cnt != 0)) {
-        const uint32_t incl = warp_incl_scan(cnt);
-        unsigned long long rank = seen + incl - cnt;
-        while (tb) {
-          const int j = __ffs(tb) - 1;
-          tb &= tb - 1;
-          if (rank >= r0) keep_ties |= 1u << j;
-          ++rank;
-        }
-        seen += __shfl_sync(0xffffffffu, incl, 31);
+  // The rule per warp from the ties of T in the warps before it (h.wtie):
+  // all masked, all kept, or the one warp where the cut falls ranks its ties.
+  auto write_ranked = [&]() {
+    int rule = kKeepAll;
+    unsigned long long seen = 0;  // ties of T before this warp's next vector (straddling warp)
+    if (!keepall) {
+      if (r0 == 0) {
+        rule = kTiesKept;
+      } else {
+        unsigned long long pre = 0;
+        for (int w = 0; w < warp; ++w) pre += h.wtie[w];
+        const unsigned long long mine = h.wtie[warp];
+        rule = (pre + mine <= r0) ? kTiesMasked : (pre >= r0 ? kTiesKept : kTiesStraddle);
+        seen = pre;
       }
+    }
+    sweep(Loads<kLoadsSimple>{}, true, [&](int e, const uint4& qin, int nv) {
+      uint32_t keep_ties = 0;  // rule == kTiesStraddle: ties of this vector that stay
+      if (rule == kTiesStraddle) {
+        uint32_t tb = eq_bits(qin, nv, T2);
+        const uint32_t cnt = __popc(tb);
+        if (__any_sync(0xffffffffu, cnt != 0)) {
+          const uint32_t incl = warp_incl_scan(cnt);
+          unsigned long long rank = seen + incl - cnt;
+          while (tb) {
+            const int j = __ffs(tb) - 1;
+            tb &= tb - 1;
+            if (rank >= r0) keep_ties |= 1u << j;
+            ++rank;
+          }
+          seen += __shfl_sync(0xffffffffu, incl, 31);
+        }
+      }
+      if (nv == 0) return;
+      uint4 q = qin;
+      if (rule != kKeepAll) {
+        auto fix = [&](uint32_t w, int j) -> uint32_t {
+          uint32_t mk;
+          if (rule == kTiesKept) mk = P::ge(w, T2);
+          else if (rule == kTiesMasked) mk = P::gt(w, T2);
+          else mk = P::gt(w, T2) | bits_word_mask<KB>(keep_ties, j);
+          return (w & mk) | (NEG2 & ~mk);
+        };
+        q.x = fix(q.x, 0);
+        q.y = fix(q.y, 1);
+        q.z = fix(q.z, 2);
+        q.w = fix(q.w, 3);
+      }
+      if (nv == VEC && vec_out) {
+        st_global_hint(orow + e, q, pol_first);
+      } else {
+  #pragma unroll
+        for (int j = 0; j < VEC; ++j)
+          if (j < nv) orow[e + j] = vec_elem<DT>(q, j);
+      }
+    });
+  };
+  const bool ranked = keepall || r0_known && (r0 == 0 || have_wtie);
+  if (ranked) {
+    write_ranked();
+    return;
+  }
+  // Ties of T are written as kept while each warp records their positions,
+  // in index order (lanes hold consecutive vectors, warps consecutive
+  // sixteenths); the first r0 of them then become -inf.  Far too many ties
+  // for the records: the counts are exact all the same, so the ranked write
+  // runs again.
+  constexpr int kTieCap = (int)(kApplyBigBytes / 4) / kWarps;
+  uint32_t* tpos = reinterpret_cast<uint32_t*>(big) + warp * kTieCap;
+  uint32_t wn = 0;  // warp-uniform
+  sweep(Loads<kLoadsSimple>{}, true, [&](int e, const uint4& qin, int nv) {
+    uint32_t tb = eq_bits(qin, nv, T2);
+    const uint32_t cnt = __popc(tb);
+    if (__any_sync(0xffffffffu, cnt != 0)) {
+      const uint32_t incl = warp_incl_scan(cnt);
+      uint32_t slot = wn + incl - cnt;
+      while (tb) {
+        const int j = __ffs(tb) - 1;
+        tb &= tb - 1;
+        if (slot < (uint32_t)kTieCap) tpos[slot] = (uint32_t)(e + j);
+        ++slot;
+      }
+      wn += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (nv == 0) return;
     uint4 q = qin;
-    if (rule != kKeepAll) {
-      auto fix = [&](uint32_t w, int j) -> uint32_t {
-        uint32_t mk;
-        if (rule == kTiesKept) mk = P::ge(w, T2);
-        else if (rule == kTiesMasked) mk = P::gt(w, T2);
-        else mk = P::gt(w, T2) | bits_word_mask<KB>(keep_ties, j);
-        return (w & mk) | (NEG2 & ~mk);
-      };
-      q.x = fix(q.x, 0);
-      q.y = fix(q.y, 1);
-      q.z = fix(q.z, 2);
-      q.w = fix(q.w, 3);
-    }
+    auto keep_ge = [&](uint32_t w) -> uint32_t {
+      const uint32_t mk = P::ge(w, T2);
+      return (w & mk) | (NEG2 & ~mk);
+    };
+    q.x = keep_ge(q.x);
+    q.y = keep_ge(q.y);
+    q.z = keep_ge(q.z);
+    q.w = keep_ge(q.w);
     if (nv == VEC && vec_out) {
       st_global_hint(orow + e, q, pol_first);
     } else {
@@ -1324,6 +1360,22 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         if (j < nv) orow[e + j] = vec_elem<DT>(q, j);
     }
   });
+  if (lane == 0) h.wtie[warp] = wn;
+  __syncthreads();
+  unsigned long long all = 0, pre = 0;
+  bool overflow = false;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) pre += h.wtie[w];
+    all += h.wtie[w];
+    overflow |= h.wtie[w] > (uint32_t)kTieCap;
+  }
+  if (!r0_known) r0 = all - 1ull;  // only the last sorted position survives: the last element equal to the max
+  if (overflow) {
+    write_ranked();
+    return;
+  }
+  for (uint32_t j = lane; j < wn; j += 32)
+    if (pre + j < r0) orow[tpos[j]] = D::kNegInf;
 }
 
 template <int DT>
