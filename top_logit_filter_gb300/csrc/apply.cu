@@ -497,14 +497,14 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   // before anything is processed; pre(q, head_vector, tail_vector) then runs
   // in every thread (it may synchronise the CTA), and f sees the row as in
   // sweep().
-  auto sweep_pre = [&](auto U_c, auto&& pre, auto&& f) {
+  auto sweep_pre = [&](auto U_c, auto&& pre, auto&& f, bool last = false) {
     constexpr int U = decltype(U_c)::value;
     uint4 q[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int v = wb + u * 32 + lane;
       q[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
-      if (v < we) q[u] = __ldcg(xv + v);
+      if (v < we) q[u] = last ? ld_global_hint(xv + v, pol_first) : __ldcg(xv + v);
     }
     const uint4 hq = load_partial(0, (warp == 0 && lane == 0) ? head : 0);
     const uint4 tq = load_partial(head + nvec * VEC, (warp == kWarps - 1 && lane == 0) ? tail : 0);
@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       for (int u = 0; u < U; ++u) {
         const int v = wb + (s0 + U + u) * 32 + lane;
         qn[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
-        if (v < we) qn[u] = __ldcg(xv + v);
+        if (v < we) qn[u] = last ? ld_global_hint(xv + v, pol_first) : __ldcg(xv + v);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -1329,9 +1329,11 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   uint32_t* tpos = reinterpret_cast<uint32_t*>(big) + warp * kTieCap;
   uint32_t wn = 0;  // warp-uniform
   sweep(Loads<kLoadsSimple>{}, true, [&](int e, const uint4& qin, int nv) {
-    uint32_t tb = eq_bits(qin, nv, T2);
-    const uint32_t cnt = __popc(tb);
-    if (__any_sync(0xffffffffu, cnt != 0)) {
+    // a packed equality test first: vectors holding a tie are rare
+    const bool maybe = (P::eq(qin.x, T2) | P::eq(qin.y, T2) | P::eq(qin.z, T2) | P::eq(qin.w, T2)) != 0u;
+    if (__any_sync(0xffffffffu, maybe)) {
+      uint32_t tb = maybe ? eq_bits(qin, nv, T2) : 0u;
+      const uint32_t cnt = __popc(tb);
       const uint32_t incl = warp_incl_scan(cnt);
       uint32_t slot = wn + incl - cnt;
       while (tb) {
