@@ -24,17 +24,22 @@
 //   2. the k-th largest vector maximum lower-bounds the row's k-th largest
 //      element (k distinct elements reach it); its bucket floor L decides
 //      candidacy.  Pass B tests every vector with one packed ">= L" compare
-//      and appends the few elements >= L to its warp's list;
+//      and appends the few elements >= L, with their positions, to its
+//      warp's list.  For small k the first load group of every warp gives
+//      the bound and pass A collects the candidates itself;
 //   3. the selection runs on the lists alone: the k-th largest key by counts,
 //      then the top-p cut by probability mass (2^-40 fixed point; for 16-bit
 //      dtypes an exact per-key histogram, so mass = count x exp(value - max)).
-// Rows with top-p only (fp16 / bf16) take the window path:
+// bf16 rows with top-p only take the mass-table path: pass A counts every
+// element per key in a table of the keys that can carry mass (a few
+// thousand), and the exact cut follows with one exponential per key.
+// fp16 rows with top-p only (and bf16 rows whose keys do not fit) take the
+// window path:
 //   1. pass A counts every element per 12-bit bucket;
 //   2. rigorous lower / upper bounds of every bucket's mass (count times the
 //      mass of its smallest / largest value) bracket the top-p cut into a
-//      window of buckets; each non-empty bucket of the window gets a block of
-//      16 per-key counters (a window that crosses zero spans thousands of
-//      nearly empty buckets, so only occupied ones get counters);
+//      window of buckets; each window bucket gets 16 per-key counters (only
+//      the occupied ones when a window crossing zero spans too many);
 //   3. pass B computes every element's mass: the row total and the mass
 //      below the window accumulate in registers (fp32 per 16-byte vector,
 //      then 2^-40 fixed point), the few elements inside the window are
@@ -44,12 +49,14 @@
 // whole row (11-bit first digit, then 5 bits for 16-bit keys or 11 + 10 for
 // fp32).
 //
-// When the cut falls inside a run of equal values, the write pass needs each
-// tie's rank in index order.  The ties of T in each warp's sixteenth are
-// known before the write pass (from the warp's candidate list or a counting
-// pass), so a warp whose ties are all masked or all kept applies one
-// compare; the single warp where the cut falls ranks its ties with warp
-// scans.
+// The write.  When the listed survivors are few, the row is filled with -inf
+// and they are scattered to their positions (ties of T ranked by position),
+// without reading the row again.  Otherwise a write pass re-reads the row:
+// with per-warp tie counts of T from the lists, a warp whose ties are all
+// masked or all kept applies one compare and only the warp where the cut
+// falls ranks its ties with warp scans; without them, the ties are written
+// as kept while every warp records their positions in index order, and the
+// first r0 then become -inf.
 #include <type_traits>
 
 #include "common.cuh"
