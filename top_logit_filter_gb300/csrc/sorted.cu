@@ -70,7 +70,7 @@ __device__ int upper_bound_fwd(const typename DType<DT>::raw* sv, int p, int V, 
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 2) sorted_kernel(const SortedArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) sorted_kernel(const SortedArgs a) {
   using D = DType<DT>;
   using raw = typename D::raw;
   constexpr int VEC = 16 / sizeof(raw);
@@ -111,6 +111,20 @@ __global__ void __launch_bounds__(kThreads, 2) sorted_kernel(const SortedArgs a)
     mbar_arrive_expect_tx(&h.mbar, bulk);
     bulk_g2s(stage, lg + c0, bulk, &h.mbar);
   }
+
+  // fill this CTA's chunk with -inf: it needs no cut, so when top-k already
+  // promises few survivors the stores drain while the cut is searched
+  auto fill_chunk = [&]() {
+    const uint32_t NEG2 = DType<DT>::kKeyBits == 16 ? ((uint32_t)D::kNegInf * 0x10001u) : (uint32_t)D::kNegInf;
+    raw* oc = o + c0;
+    const int head = ((uintptr_t)oc & 15u) ? min(n, (int)((16u - ((uintptr_t)oc & 15u)) / sizeof(raw))) : 0;
+    for (int i = tid; i < head; i += kThreads) oc[i] = D::kNegInf;
+    const int nv = (n - head) / VEC;
+    uint4* ov = reinterpret_cast<uint4*>(oc + head);
+    for (int i = tid; i < nv; i += kThreads) ov[i] = make_uint4(NEG2, NEG2, NEG2, NEG2);
+    for (int i = head + nv * VEC + tid; i < n; i += kThreads) oc[i] = D::kNegInf;
+  };
+  if (few_expected) fill_chunk();
 
   // ---- top-k boundary ([guide] §2 steps 1-3) ----
   int jk = 0;
@@ -173,16 +187,9 @@ __global__ void __launch_bounds__(kThreads, 2) sorted_kernel(const SortedArgs a)
 
   // ---- write ([guide] §2 step 8) ----
   if (V - J <= V / 8) {
-    // fill this CTA's chunk with -inf, then scatter the survivors
+    // the chunk filled with -inf (unless done above), then the survivors
     if (bulk && !mbar_wait_bounded(&h.mbar, 0, a.timeout_ns)) atomicOr(&g_device_error, 1u);
-    const uint32_t NEG2 = DType<DT>::kKeyBits == 16 ? ((uint32_t)D::kNegInf * 0x10001u) : (uint32_t)D::kNegInf;
-    raw* oc = o + c0;
-    const int head = ((uintptr_t)oc & 15u) ? min(n, (int)((16u - ((uintptr_t)oc & 15u)) / sizeof(raw))) : 0;
-    for (int i = tid; i < head; i += kThreads) oc[i] = D::kNegInf;
-    const int nv = (n - head) / VEC;
-    uint4* ov = reinterpret_cast<uint4*>(oc + head);
-    for (int i = tid; i < nv; i += kThreads) ov[i] = make_uint4(NEG2, NEG2, NEG2, NEG2);
-    for (int i = head + nv * VEC + tid; i < n; i += kThreads) oc[i] = D::kNegInf;
+    if (!few_expected) fill_chunk();
     if (C > 1) cluster_sync_all(); else __syncthreads();
     for (int j = J + (int)crank * kThreads + tid; j < V; j += C * kThreads) {
       const int v = si[j];
