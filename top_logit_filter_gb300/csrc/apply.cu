@@ -1251,7 +1251,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     const int onv = (V - ohead) / VEC;
     for (int i = tid; i < ohead; i += kThreads) orow[i] = D::kNegInf;
     uint4* ov = reinterpret_cast<uint4*>(orow + ohead);
-    for (int i = tid; i < onv; i += kThreads) ov[i] = make_uint4(NEG2, NEG2, NEG2, NEG2);
+    for (int i = tid; i < onv; i += kThreads) st_global_hint(ov + i, make_uint4(NEG2, NEG2, NEG2, NEG2), pol_first);
     for (int i = ohead + onv * VEC + tid; i < V; i += kThreads) orow[i] = D::kNegInf;
     __syncthreads();
     const int myn = (int)h.nseg[warp];
