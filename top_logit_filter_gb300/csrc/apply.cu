@@ -66,6 +66,7 @@ namespace topkp {
 
 constexpr int kBins = 4096;                  // 12-bit first digit: candidate path, key-count buckets
 constexpr int kSmallBins = 256;              // 8-bit digits over candidate lists
+constexpr int kBPT = kBins / kThreads;       // 12-bit bins each thread scans
 constexpr int kKeyBlocks = (int)(kApplyBigBytes / (16 * 4));  // 16-key count blocks of the window path
 static_assert(kApplyAuxBytes >= (size_t)kKeyBlocks * (2 + 8), "block -> bucket map and block masses");
 static_assert(2 * kBins * 8 <= (int)kApplyBigBytes, "bucket mass bounds fit the big region");
@@ -288,6 +289,17 @@ __device__ __forceinline__ unsigned long long block_sum_f(F&& val, unsigned long
 
 
 
+// Shared-memory slot of bin v in a table that thread t scans as the BPT
+// consecutive bins BPT*t .. BPT*t+BPT-1 (BPT a power of two <= 32): the low
+// bits are XORed with the bin's 32-word group, so the 32 lanes of a warp
+// reading their j-th bins hit 32 different banks.  A bijection on every
+// aligned run of BPT bins.
+template <int BPT>
+__device__ __forceinline__ uint32_t swz(uint32_t v) {
+  static_assert(BPT >= 1 && BPT <= 32 && (BPT & (BPT - 1)) == 0, "BPT");
+  return v ^ ((v >> 5) & (uint32_t)(BPT - 1));
+}
+
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -333,34 +345,52 @@ __device__ __forceinline__ uint32_t block_first_true(uint32_t lo, uint32_t hi, P
 template <int DT, typename Cnt, typename KeyOf, typename Ok>
 __device__ __forceinline__ Sel mass_cut(int n, int first, Cnt cnt, KeyOf key_of, Ok ok, const MassRef& mr, float thr,
                                         ApplyHdr& h, bool* last) {
-  const int bpt = (n + kThreads - 1) / kThreads;
+  // an odd number of bins per thread: the lanes of a warp reading their
+  // i-th bins then touch 32 different banks of a linear table
+  const int bpt = ((n + kThreads - 1) / kThreads) | 1;
   const int b0 = min(n, (int)threadIdx.x * bpt), b1 = min(n, b0 + bpt);
+  const int i0 = max(b0, first);
+  // no branch on empty bins: the unrolled iterations overlap
   unsigned long long s = 0;
 #pragma unroll 4
-  for (int i = max(b0, first); i < b1; ++i) {
-    const uint32_t c = cnt(i);
-    if (c) s += (unsigned long long)c * mass_fixed(value_of_key<DT>(key_of(i)), mr);
-  }
+  for (int i = i0; i < b1; ++i)
+    s += (unsigned long long)cnt(i) * mass_fixed(value_of_key<DT>(key_of(i)), mr);
   unsigned long long S;
   const unsigned long long ex = block_exclusive_scan(s, &S, h.ws);
   const unsigned long long target = mass_target(thr, S);
   *last = target >= S;
   if (*last) return Sel{-1, 0ull};
-  if (ex <= target && target < ex + s) {
-    unsigned long long acc = ex;
-    for (int i = max(b0, first); i < b1; ++i) {
-      const uint32_t c = cnt(i);
-      if (!c) continue;
-      const unsigned long long u = mass_fixed(value_of_key<DT>(key_of(i)), mr);
-      const unsigned long long mk = (unsigned long long)c * u;
-      if (target < acc + mk) {
-        if (ok(i)) {
+  // The warp of the one thread whose bins hold the target walks that
+  // thread's bins 32 at a time: a scan over the lanes finds the bin where
+  // the cumulative mass passes the target.
+  const int lane = (int)threadIdx.x & 31;
+  const unsigned own = __ballot_sync(0xffffffffu, ex <= target && target < ex + s);
+  if (own) {
+    const int src = __ffs(own) - 1;
+    unsigned long long acc = __shfl_sync(0xffffffffu, ex, src);
+    const int o0 = __shfl_sync(0xffffffffu, i0, src), o1 = __shfl_sync(0xffffffffu, b1, src);
+    for (int base = o0; base < o1; base += 32) {
+      const int i = base + lane;
+      unsigned long long u = 0, mk = 0;
+      if (i < o1) {
+        u = mass_fixed(value_of_key<DT>(key_of(i)), mr);
+        mk = (unsigned long long)cnt(i) * u;
+      }
+      unsigned long long incl = mk;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned cross = __ballot_sync(0xffffffffu, i < o1 && target < acc + incl);
+      if (cross) {
+        if (lane == __ffs(cross) - 1 && ok(i)) {
           h.sel_bin = (int)key_of(i);
-          h.sel_off = u ? (target - acc) / u : 0ull;
+          h.sel_off = u ? (target - (acc + incl - mk)) / u : 0ull;
         }
         break;
       }
-      acc += mk;
+      acc += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
   return finish_select(h);
@@ -373,6 +403,22 @@ using CandKey = typename std::conditional<DType<DT>::kKeyBits == 16, uint16_t, u
 
 template <int N>
 using Loads = std::integral_constant<int, N>;
+// How a pass reads the row: through the non-coherent path, through L2 only,
+// or (the final read) with an L2 evict-first hint.
+enum ReadKind { kReadNc, kReadCg, kReadLast };
+template <int R>
+using ReadAs = std::integral_constant<int, R>;
+
+// 16 bytes through the non-coherent path, not allocated in L1.  Only passes
+// that end before the write pass starts use it, so even in place no CTA reads
+// a logit it has already overwritten.
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
@@ -450,6 +496,13 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     for (int i = tid; i < kMassBins / 4; i += kThreads) reinterpret_cast<uint4*>(kcount)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
 
+  // One 16-byte vector of the row, read as the pass's load kind says.
+  auto load_vec = [&](auto L_c, const uint4* a) -> uint4 {
+    constexpr int L = decltype(L_c)::value;
+    if constexpr (L == kReadLast) return ld_global_hint(a, pol_first);
+    else if constexpr (L == kReadNc) return ld_nc_v4(a);
+    else return __ldcg(a);
+  };
   // n elements from row offset e0 as a vector, the rest -inf
   auto load_partial = [&](int e0, int n) -> uint4 {
     uint32_t w[4] = {NEG2, NEG2, NEG2, NEG2};
@@ -471,8 +524,8 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   // order, q = the 16 bytes at row offsets e .. e+VEC-1 with nv of them valid
   // (-inf in the others, which never exceeds a valid element and has zero
   // mass; nv = 0 on idle lanes).  All lanes of a warp call f together.  U
-  // vectors per lane are in flight; last: the final read of the row.
-  auto sweep = [&](auto U_c, bool last, auto&& f) {
+  // vectors per lane are in flight, read as L_c (a ReadKind) says.
+  auto sweep = [&](auto U_c, auto L_c, auto&& f) {
     constexpr int U = decltype(U_c)::value;
     if (warp == 0 && head > 0) {
       const uint4 q = load_partial(0, lane == 0 ? head : 0);
@@ -484,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       for (int u = 0; u < U; ++u) {
         const int v = wb + (s0 + u) * 32 + lane;
         q[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
-        if (v < we) q[u] = last ? ld_global_hint(xv + v, pol_first) : __ldcg(xv + v);
+        if (v < we) q[u] = load_vec(L_c, xv + v);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -504,14 +557,14 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   // before anything is processed; pre(q, head_vector, tail_vector) then runs
   // in every thread (it may synchronise the CTA), and f sees the row as in
   // sweep().
-  auto sweep_pre = [&](auto U_c, auto&& pre, auto&& f, bool last = false) {
+  auto sweep_pre = [&](auto U_c, auto L_c, auto&& pre, auto&& f) {
     constexpr int U = decltype(U_c)::value;
     uint4 q[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int v = wb + u * 32 + lane;
       q[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
-      if (v < we) q[u] = last ? ld_global_hint(xv + v, pol_first) : __ldcg(xv + v);
+      if (v < we) q[u] = load_vec(L_c, xv + v);
     }
     const uint4 hq = load_partial(0, (warp == 0 && lane == 0) ? head : 0);
     const uint4 tq = load_partial(head + nvec * VEC, (warp == kWarps - 1 && lane == 0) ? tail : 0);
@@ -524,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       for (int u = 0; u < U; ++u) {
         const int v = wb + (s0 + U + u) * 32 + lane;
         qn[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
-        if (v < we) qn[u] = last ? ld_global_hint(xv + v, pol_first) : __ldcg(xv + v);
+        if (v < we) qn[u] = load_vec(L_c, xv + v);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -539,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     if (warp == kWarps - 1 && tail > 0) f(head + nvec * VEC, tq, lane == 0 ? tail : 0);
   };
   auto each_elem = [&](auto&& g) {
-    sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
+    sweep(Loads<kLoadsHeavy>{}, ReadAs<kReadNc>{}, [&](int, const uint4& q, int nv) {
 #pragma unroll
       for (int j = 0; j < VEC; ++j)
         if (j < nv) g(vec_elem<DT>(q, j));
@@ -591,16 +644,16 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   if (single) {
     uint32_t L2 = 0;
     sweep_pre(
-        Loads<kLoadsHeavy>{},
+        Loads<kLoadsHeavy>{}, ReadAs<kReadNc>{},
         [&](const uint4 (&q)[kLoadsHeavy], const uint4& hq, const uint4& tq) {
 #pragma unroll
           for (int u = 0; u < kLoadsHeavy; ++u)
-            if (wb + u * 32 + lane < we) atomicAdd(&hist[vmax_key(q[u]) >> SHB], 1u);
-          if (warp == 0 && lane == 0 && head > 0) atomicAdd(&hist[vmax_key(hq) >> SHB], 1u);
-          if (warp == kWarps - 1 && lane == 0 && tail > 0) atomicAdd(&hist[vmax_key(tq) >> SHB], 1u);
+            if (wb + u * 32 + lane < we) atomicAdd(&hist[swz<kBPT>(vmax_key(q[u]) >> SHB)], 1u);
+          if (warp == 0 && lane == 0 && head > 0) atomicAdd(&hist[swz<kBPT>(vmax_key(hq) >> SHB)], 1u);
+          if (warp == kWarps - 1 && lane == 0 && tail > 0) atomicAdd(&hist[swz<kBPT>(vmax_key(tq) >> SHB)], 1u);
           __syncthreads();
           const int lb = select_desc_f<kBins / kThreads>(
-              [&](int j) -> unsigned long long { return hist[(kBins / kThreads) * tid + j]; },
+              [&](int j) -> unsigned long long { return hist[swz<kBPT>(kBPT * tid + j)]; },
               (unsigned long long)kv, h).bin;
           // fewer than k vectors in the groups: every element (the lists overflow)
           Lkey = lb > 0 ? (uint32_t)lb << SHB : order_key<DT>(D::kNegInf) + 1u;
@@ -611,11 +664,11 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
           append_ge(e, q, nv, L2);
         });
   } else if (topk && !generic_only) {
-    sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) {
+    sweep(Loads<kLoadsSimple>{}, ReadAs<kReadNc>{}, [&](int, const uint4& q, int nv) {
       if (nv) {
         const uint32_t key = vmax_key(q);
         kmax = max(kmax, key);
-        atomicAdd(&hist[key >> SHB], 1u);
+        atomicAdd(&hist[swz<kBPT>(key >> SHB)], 1u);
       }
     });
   } else if (masstab) {
@@ -634,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     if constexpr (KB == 16) {
       uint32_t ta = 0, tb = 0, tfloor = 0;
       sweep_pre(
-          Loads<kLoadsHeavy>{},
+          Loads<kLoadsHeavy>{}, ReadAs<kReadCg>{},
           [&](const uint4 (&q)[kLoadsHeavy], const uint4& hq, const uint4& tq) {
             uint32_t km = max(vmax_key(hq), vmax_key(tq));
 #pragma unroll
@@ -694,18 +747,18 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     }
   } else if (window && DT != TOPKP_BF16) {
     if constexpr (KB == 16) {
-      sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
+      sweep(Loads<kLoadsHeavy>{}, ReadAs<kReadCg>{}, [&](int, const uint4& q, int nv) {
         if (nv) kmax = max(kmax, vmax_key(q));
         const uint32_t kp[4] = {order_keys2(q.x), order_keys2(q.y), order_keys2(q.z), order_keys2(q.w)};
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
           const uint32_t key = (j & 1) ? (kp[j >> 1] >> 16) : (kp[j >> 1] & 0xffffu);
-          if (j < nv) atomicAdd(&hist[key >> SHB], 1u);
+          if (j < nv) atomicAdd(&hist[swz<kBPT>(key >> SHB)], 1u);
         }
       });
     }
   } else if (!keepall) {
-    sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) {
+    sweep(Loads<kLoadsSimple>{}, ReadAs<kReadNc>{}, [&](int, const uint4& q, int nv) {
       if (nv) kmax = max(kmax, vmax_key(q));
     });
   }
@@ -741,20 +794,20 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         if (tid < kWarps) h.nseg[tid] = 0;
         if (tid == 0) h.over = 0;
         __syncthreads();
-        sweep(Loads<kLoadsSimple>{}, false, [&](int, const uint4& q, int nv) {
-          if (nv) atomicAdd(&hist[vmax_key(q) >> SHB], 1u);
+        sweep(Loads<kLoadsSimple>{}, ReadAs<kReadNc>{}, [&](int, const uint4& q, int nv) {
+          if (nv) atomicAdd(&hist[swz<kBPT>(vmax_key(q) >> SHB)], 1u);
         });
         __syncthreads();
       }
     }
     if (!listed) {
       const int lb = select_desc_f<kBins / kThreads>(
-          [&](int j) -> unsigned long long { return hist[(kBins / kThreads) * tid + j]; }, (unsigned long long)kv, h).bin;
+          [&](int j) -> unsigned long long { return hist[swz<kBPT>(kBPT * tid + j)]; }, (unsigned long long)kv, h).bin;
       if (lb > 0) {
         // pass B (from L2): every element >= L joins its warp's list
         Lkey = (uint32_t)lb << SHB;
         const uint32_t L2 = P::splat((uint32_t)raw_of_key<DT>(Lkey));
-        sweep(Loads<kLoadsSimple>{}, false, [&](int e, const uint4& q, int nv) { append_ge(e, q, nv, L2); });
+        sweep(Loads<kLoadsSimple>{}, ReadAs<kReadNc>{}, [&](int e, const uint4& q, int nv) { append_ge(e, q, nv, L2); });
         __syncwarp();
         if (lane == 0 && h.nseg[warp] > (uint32_t)CAPW) {
           h.nseg[warp] = CAPW;
@@ -775,20 +828,19 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
           // exact per-key counts over [L, max]: a 16-bit key is a value
           for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
           __syncthreads();
-          each_own([&](uint32_t key) { atomicAdd(&hist[key - Lkey], 1u); });
+          each_own([&](uint32_t key) { atomicAdd(&hist[swz<kBPT>(key - Lkey)], 1u); });
           __syncthreads();
-          constexpr int BPT = kBins / kThreads;
-          auto cnt = [&](int j) -> unsigned long long { return hist[BPT * tid + j]; };
-          const int bk = select_desc_f<BPT>(cnt, (unsigned long long)kv, h).bin;
+          auto cnt = [&](int j) -> unsigned long long { return hist[swz<kBPT>(kBPT * tid + j)]; };
+          const int bk = select_desc_f<kBPT>(cnt, (unsigned long long)kv, h).bin;
           T = Lkey + (uint32_t)bk;
           if (topp) {
             bool last;
             const Sel sp = mass_cut<DT>(
-                (int)(gmax - Lkey) + 1, bk, [&](int i) { return hist[i]; },
+                (int)(gmax - Lkey) + 1, bk, [&](int i) { return hist[swz<kBPT>(i)]; },
                 [&](int i) { return Lkey + (uint32_t)i; }, [](int) { return true; }, mr, thr, h, &last);
             if (last) {
               cut_last = true;
-              r0 = hist[gmax - Lkey] - 1ull;
+              r0 = hist[swz<kBPT>(gmax - Lkey)] - 1ull;
             } else {
               T = (uint32_t)sp.bin;
               r0 = sp.off;
@@ -938,12 +990,12 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       // fall back to the window path: it needs the bucket counts
       __syncthreads();
       if constexpr (KB == 16) {
-        sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
+        sweep(Loads<kLoadsHeavy>{}, ReadAs<kReadCg>{}, [&](int, const uint4& q, int nv) {
           const uint32_t kp[4] = {order_keys2(q.x), order_keys2(q.y), order_keys2(q.z), order_keys2(q.w)};
 #pragma unroll
           for (int j = 0; j < VEC; ++j) {
             const uint32_t key = (j & 1) ? (kp[j >> 1] >> 16) : (kp[j >> 1] & 0xffffu);
-            if (j < nv) atomicAdd(&hist[key >> SHB], 1u);
+            if (j < nv) atomicAdd(&hist[swz<kBPT>(key >> SHB)], 1u);
           }
         });
       }
@@ -963,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
 #pragma unroll
     for (int j = 0; j < BPT; ++j) {
       const int b = BPT * tid + j;
-      const uint32_t c = hist[b];
+      const uint32_t c = hist[swz<kBPT>(b)];
       unsigned long long lo = 0, hi = 0;
       if (c) {
         const unsigned long long m0 = mass_fixed(value_of_key<DT>((uint32_t)b << SHB), mr);
@@ -1016,7 +1068,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
 #pragma unroll
     for (int j = 0; j < BPT; ++j) {
       const int b = BPT * tid + j;
-      occ += (b >= w0 && b <= w1 && (direct || hist[b] != 0)) ? 1u : 0u;
+      occ += (b >= w0 && b <= w1 && (direct || hist[swz<kBPT>(b)] != 0)) ? 1u : 0u;
     }
     unsigned long long nocc;
     uint32_t id = (uint32_t)block_exclusive_scan(occ, &nocc, h.ws);
@@ -1024,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
 #pragma unroll
       for (int j = 0; j < BPT; ++j) {
         const int b = BPT * tid + j;
-        if (b >= w0 && b <= w1 && (direct || hist[b] != 0)) {
+        if (b >= w0 && b <= w1 && (direct || hist[swz<kBPT>(b)] != 0)) {
           bucket_of[id] = (uint16_t)b;
           block_of[b] = id++;
         } else {
@@ -1046,7 +1098,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       constexpr int kRun = 4;
       const uint32_t LO2 = P::splat((uint32_t)raw_of_key<DT>((uint32_t)w0 << SHB));
       const uint32_t HI2 = P::splat((uint32_t)raw_of_key<DT>(((uint32_t)w1 << SHB) | ((1u << SHB) - 1u)));
-      sweep(Loads<kLoadsHeavy>{}, false, [&](int, const uint4& q, int nv) {
+      sweep(Loads<kLoadsHeavy>{}, ReadAs<kReadCg>{}, [&](int, const uint4& q, int nv) {
         // two values per word: one packed fma, two exponentials, one packed
         // add; the -inf padding has zero mass, so no element mask is needed
         float2 sv = make_float2(0.0f, 0.0f);
@@ -1281,7 +1333,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         seen = pre;
       }
     }
-    sweep(Loads<kLoadsSimple>{}, true, [&](int e, const uint4& qin, int nv) {
+    sweep(Loads<kLoadsSimple>{}, ReadAs<kReadLast>{}, [&](int e, const uint4& qin, int nv) {
       uint32_t keep_ties = 0;  // rule == kTiesStraddle: ties of this vector that stay
       if (rule == kTiesStraddle) {
         uint32_t tb = eq_bits(qin, nv, T2);
@@ -1335,7 +1387,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   constexpr int kTieCap = (int)(kApplyBigBytes / 4) / kWarps;
   uint32_t* tpos = reinterpret_cast<uint32_t*>(big) + warp * kTieCap;
   uint32_t wn = 0;  // warp-uniform
-  sweep(Loads<kLoadsSimple>{}, true, [&](int e, const uint4& qin, int nv) {
+  sweep(Loads<kLoadsSimple>{}, ReadAs<kReadLast>{}, [&](int e, const uint4& qin, int nv) {
     // a packed equality test first: vectors holding a tie are rare
     const bool maybe = (P::eq(qin.x, T2) | P::eq(qin.y, T2) | P::eq(qin.z, T2) | P::eq(qin.w, T2)) != 0u;
     if (__any_sync(0xffffffffu, maybe)) {
