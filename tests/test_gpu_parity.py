@@ -223,3 +223,28 @@ def test_workload3_mode_variants_full_size(tk, mode):
         _, info = O.apply_row(w["x"][b], dt, None if p is None else p[b], None if k is None else int(k[b]))
         flips += compare_row(out[b], w["x"][b], info, dt, where=f"{mode} row {b}")
     print(f"{mode}: {flips} top-p flips inside the band")
+
+
+@pytest.mark.parametrize("dtype", ("f16", "bf16"))
+def test_top_p_cut_among_signed_zeros(tk, monkeypatch, dtype):
+    """Top-p-only rows whose cut falls inside a run of zeros, -0 and +0
+    mixed: the two compare equal, so they rank as ties in index order and
+    the first kept zero may be either."""
+    rng = np.random.default_rng(17)
+    V = 4000
+    vals = np.array([-1.0, -0.0, 0.0, 1.0, 2.0], dtype=np.float32)
+    ps = np.linspace(0.80, 0.98, 16)
+    x = np.stack([to_raw(rng.permutation(np.repeat(vals, V // len(vals))), dtype) for _ in ps])
+    p = to_raw(ps, dtype)
+    # the oracle's first kept element is -0 in some rows and +0 in others
+    cut_bits = set()
+    for b in range(len(ps)):
+        _, info = O.apply_row(x[b], dtype, p[b], None)
+        first = info.idx[np.argmax(info.kept)]
+        cut_bits.add(int(bits(x[b][first:first + 1], dtype)[0]))
+    assert {int(bits(to_raw(np.array([-0.0], np.float32), dtype), dtype)[0]),
+            int(bits(to_raw(np.array([0.0], np.float32), dtype), dtype)[0])} <= cut_bits
+    for plan in PLANS:
+        monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
+        out = _run_apply(tk, x, dtype, p, None)
+        _check_all(out, x, dtype, p, None, f"{dtype} signed zeros plan={plan!r}")

@@ -93,6 +93,7 @@ struct __align__(16) ApplyHdr {
   uint32_t mt_a, mt_b, mt_floor, mt_k0;  // mass-table path: bin = a - mag (x < 0) or b + mag (x >= 0),
   int mt_qn;                             // mag clamped to >= floor; qn = bin of the negative floor;
   uint32_t mt_lump;                      // k0 = provisional max key; lump: floors hold zero-equal keys
+  uint32_t slot;                         // block_first_true scratch
 };
 static_assert(sizeof(ApplyHdr) <= kApplyHdrBytes, "header too large");
 
@@ -460,7 +461,11 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   const bool topk = a.k != nullptr && kv >= 1 && kv <= V - 1;
   const bool topp = a.p != nullptr;
   const bool keepall = !topk && !topp;
-  const bool window = !topk && topp && KB == 16 && !generic_only;
+  const float thr = topp ? top_p_threshold<DT>(a.p, row) : 0.0f;
+  // top-p alone with threshold 0 masks only elements of zero mass: the cut
+  // follows from the row max, and pass A reads the max only
+  const bool p_zero = !topk && topp && !(thr > 0.0f) && !generic_only;
+  const bool window = !topk && topp && !p_zero && KB == 16 && !generic_only;
   const bool masstab = window && DT == TOPKP_BF16;
   const bool in_place = reinterpret_cast<const void*>(xr) == reinterpret_cast<const void*>(orow);
   if (keepall && in_place) return;  // nothing to filter, nothing to move
@@ -772,7 +777,6 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   bool done = keepall;          // cut found
   bool have_wtie = false;       // h.wtie holds the ties of T per warp
   bool r0_known = true;         // cut_last: r0 already counted
-  const float thr = topp ? top_p_threshold<DT>(a.p, row) : 0.0f;
   const uint32_t gmax = h.maxkey;
   const MassRef mr(value_of_key<DT>(gmax));
 
@@ -1087,6 +1091,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       for (int i = tid; i < (int)nocc * 4; i += kThreads) kc4[i] = make_uint4(0, 0, 0, 0);
       __syncthreads();
       const uint32_t wkey0 = (uint32_t)w0 << SHB;
+      const uint32_t nwin = (uint32_t)nocc * 16u;  // counters in use
       // pass B (from L2): row mass and mass below the window (fp32 per
       // vector, then fixed point), per-key counts inside the window.  Window
       // membership is a float compare: key order is value order.
@@ -1130,7 +1135,8 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
           for (int j = 0; j < VEC; ++j) {
             if (inwin & (1u << j)) {
               const uint32_t key = (j & 1) ? (kp[j >> 1] >> 16) : (kp[j >> 1] & 0xffffu);
-              atomicAdd(&kcount[direct ? key - wkey0 : block_of[key >> SHB] * 16 + (key & 15u)], 1u);
+              const uint32_t ix = direct ? key - wkey0 : block_of[key >> SHB] * 16 + (key & 15u);
+              if (ix < nwin) atomicAdd(&kcount[ix], 1u);  // always: key order is value order
             }
           }
         }
@@ -1203,6 +1209,19 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         }
       }
     }
+  }
+
+  // ------------------------------------- top-p alone with threshold 0
+  // Masked iff the cumulative mass is <= 0: exactly the elements of zero
+  // fixed-point mass, the smallest values up to a key that the row max
+  // alone fixes (mass grows with the key).  The first key of non-zero mass
+  // is the cut, with every tie kept.  A row max that is not finite takes
+  // the generic path.
+  if (!done && p_zero && isfinite(value_of_key<DT>(gmax))) {
+    T = block_first_true(order_key<DT>(D::kNegInf) + 1u, gmax,
+                         [&](uint32_t key) { return mass_fixed(value_of_key<DT>(key), mr) > 0ull; }, &h.slot);
+    r0 = 0;
+    done = true;
   }
 
   // ------------------------------------------------------ generic path
