@@ -771,6 +771,34 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   if (lane == 0) atomicMax(&h.maxkey, kmax);
   __syncthreads();
 
+  // Rows whose survivors number at most k <= V/8 end in the -inf fill and
+  // scatter write (unless the cut's ties overflow the ranking).  Their fill
+  // starts now, as bulk copies of a -inf block in shared memory (the window
+  // path's region, unused by these rows) that run during the selection;
+  // the write then waits for them and scatters the survivors.
+  constexpr int kFillBlock = 8192;
+  static_assert(kFillBlock <= (int)kApplyAuxBytes, "fill block fits the aux region");
+  const bool early_fill = topk && !generic_only && kv <= V / 8 &&
+                          reinterpret_cast<const void*>(orow) != reinterpret_cast<const void*>(xr);
+  if (early_fill) {
+    uint4* negs = reinterpret_cast<uint4*>(aux);
+    for (int i = tid; i < kFillBlock / 16; i += kThreads) negs[i] = make_uint4(NEG2, NEG2, NEG2, NEG2);
+    fence_proxy_async_shared();
+    __syncthreads();
+    const uintptr_t oaddr = reinterpret_cast<uintptr_t>(orow);
+    const int ohead = min(V, (int)(((16u - (uint32_t)(oaddr & 15u)) & 15u) / (uint32_t)sizeof(raw)));
+    const int onv = (V - ohead) / VEC;
+    for (int i = tid; i < ohead; i += kThreads) orow[i] = D::kNegInf;
+    for (int i = ohead + onv * VEC + tid; i < V; i += kThreads) orow[i] = D::kNegInf;
+    if (tid == 0) {
+      unsigned char* dst = reinterpret_cast<unsigned char*>(orow + ohead);
+      const long long body = (long long)onv * 16;
+      for (long long off = 0; off < body; off += kFillBlock)
+        bulk_store_s2g(dst + off, negs, (uint32_t)min(body - off, (long long)kFillBlock));
+      bulk_commit_group();
+    }
+  }
+
   uint32_t T = 0;               // cut key
   unsigned long long r0 = 0;    // ties of T masked, in index order
   bool cut_last = false;        // top-p keeps only the last sorted position
@@ -1315,16 +1343,27 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   const uint32_t T2 = P::splat((uint32_t)raw_of_key<DT>(T));
   __syncthreads();
 
+  if (early_fill) {
+    // the early fill has landed before any write of this row
+    if (tid == 0) {
+      bulk_wait_all();
+      fence_proxy_async_global();
+    }
+    __syncthreads();
+  }
+
   // ---- write: the listed survivors over a -inf row ([guide] §2 step 8) ----
   if (h.fill) {
-    const uintptr_t oaddr = reinterpret_cast<uintptr_t>(orow);
-    const int ohead = min(V, (int)(((16u - (uint32_t)(oaddr & 15u)) & 15u) / (uint32_t)sizeof(raw)));
-    const int onv = (V - ohead) / VEC;
-    for (int i = tid; i < ohead; i += kThreads) orow[i] = D::kNegInf;
-    uint4* ov = reinterpret_cast<uint4*>(orow + ohead);
-    for (int i = tid; i < onv; i += kThreads) st_global_hint(ov + i, make_uint4(NEG2, NEG2, NEG2, NEG2), pol_first);
-    for (int i = ohead + onv * VEC + tid; i < V; i += kThreads) orow[i] = D::kNegInf;
-    __syncthreads();
+    if (!early_fill) {
+      const uintptr_t oaddr = reinterpret_cast<uintptr_t>(orow);
+      const int ohead = min(V, (int)(((16u - (uint32_t)(oaddr & 15u)) & 15u) / (uint32_t)sizeof(raw)));
+      const int onv = (V - ohead) / VEC;
+      for (int i = tid; i < ohead; i += kThreads) orow[i] = D::kNegInf;
+      uint4* ov = reinterpret_cast<uint4*>(orow + ohead);
+      for (int i = tid; i < onv; i += kThreads) st_global_hint(ov + i, make_uint4(NEG2, NEG2, NEG2, NEG2), pol_first);
+      for (int i = ohead + onv * VEC + tid; i < V; i += kThreads) orow[i] = D::kNegInf;
+      __syncthreads();
+    }
     const int myn = (int)h.nseg[warp];
     const uint32_t tcut = h.tie_cut;
     for (int j = lane; j < myn; j += 32) {
