@@ -790,10 +790,11 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     const int onv = (V - ohead) / VEC;
     for (int i = tid; i < ohead; i += kThreads) orow[i] = D::kNegInf;
     for (int i = ohead + onv * VEC + tid; i < V; i += kThreads) orow[i] = D::kNegInf;
-    if (tid == 0) {
+    if (lane == 0) {
+      // lane 0 of every warp issues every kWarps-th block
       unsigned char* dst = reinterpret_cast<unsigned char*>(orow + ohead);
       const long long body = (long long)onv * 16;
-      for (long long off = 0; off < body; off += kFillBlock)
+      for (long long off = (long long)warp * kFillBlock; off < body; off += (long long)kWarps * kFillBlock)
         bulk_store_s2g(dst + off, negs, (uint32_t)min(body - off, (long long)kFillBlock));
       bulk_commit_group();
     }
@@ -1345,7 +1346,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
 
   if (early_fill) {
     // the early fill has landed before any write of this row
-    if (tid == 0) {
+    if (lane == 0) {
       bulk_wait_all();
       fence_proxy_async_global();
     }
