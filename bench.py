@@ -47,6 +47,22 @@ def _dist():
     return ws, rank, local
 
 
+def _max_over_ranks(value: float, ws: int, device) -> float:
+    """The largest value over all ranks: a job's time is its slowest rank's."""
+    if ws <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_rows_per_s(ws: int, rows: int, steps: int, total_s: float) -> float:
+    """Whole-job throughput of weak-scaling replicas: every rank filters
+    `rows` rows per step, and the job takes the slowest rank's time."""
+    return ws * rows * steps / total_s
+
+
 def _peak_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -224,12 +240,9 @@ def run_ours(args):
     tk.device_status(dev)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_s = sum(step_ms) / 1e3
-    if ws > 1:
-        t = torch.tensor([total_s], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = _max_over_ranks(total_s, ws, dev)
     ms_per_step = 1e3 * total_s / args.steps
-    value = ws * B * args.steps / total_s
+    value = _job_rows_per_s(ws, B, args.steps, total_s)
 
     # roofline of the filter kernel: one launch per step
     alg_bytes = B * V * 2 * 2
@@ -261,7 +274,8 @@ def run_ours(args):
     e2e_s = e0.elapsed_time(e1) / 1e3
     h2d = hx.numel() * hx.element_size() + hp.numel() * hp.element_size() + hk.numel() * hk.element_size()
     d2h = hout.numel() * hout.element_size()
-    e2e = {"value": ws * B * e2e_steps / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+    e2e_s = _max_over_ranks(e2e_s, ws, dev)
+    e2e = {"value": _job_rows_per_s(ws, B, e2e_steps, e2e_s), "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "steps": e2e_steps}
 
     if rank == 0:
