@@ -118,8 +118,8 @@ __device__ __forceinline__ float2 add2_f32(float2 a, float2 b) {
   return make_float2(r0, r1);
 }
 // A finite float >= 0 below 2^63 rounded to the nearest integer, ties to
-// even, in integer ALU operations.  (The library conversion to a 64-bit
-// integer runs on the FP64 pipe, which this GPU keeps very narrow.)
+// even, with one fp32 add or one shift.  (The library conversion to a
+// 64-bit integer runs on the FP64 pipe, which this GPU keeps very narrow.)
 __host__ __device__ __forceinline__ uint32_t float_bits(float f) {
 #ifdef __CUDA_ARCH__
   return __float_as_uint(f);
@@ -130,18 +130,12 @@ __host__ __device__ __forceinline__ uint32_t float_bits(float f) {
 #endif
 }
 __host__ __device__ __forceinline__ unsigned long long f2ull_rn(float f) {
+  // Below 2^23, adding 2^23 leaves the integer part in the mantissa, rounded
+  // to nearest with ties to even by the fp32 add itself.  From 2^23 on, a
+  // float is an integer: its mantissa shifted by the exponent.
+  if (f < 8388608.0f) return (unsigned long long)(float_bits(f + 8388608.0f) - 0x4b000000u);
   const uint32_t b = float_bits(f);
-  const uint32_t be = b >> 23;                  // biased exponent (sign is 0)
-  if (be == 0) return 0ull;                     // zero or subnormal (< 2^-126)
-  const uint32_t m = (b & 0x7fffffu) | 0x800000u;
-  const int e = (int)be - 150;                  // f = m * 2^e
-  if (e >= 0) return (unsigned long long)m << e;
-  const int k = -e;
-  if (k > 24) return 0ull;                      // m / 2^k < 1/2
-  const uint32_t q = m >> k;
-  const uint32_t rem = m & ((1u << k) - 1u);
-  const uint32_t half = 1u << (k - 1);
-  return (unsigned long long)(q + ((rem > half || (rem == half && (q & 1u))) ? 1u : 0u));
+  return (unsigned long long)((b & 0x7fffffu) | 0x800000u) << ((b >> 23) - 150u);
 }
 __device__ __forceinline__ unsigned long long mass_fixed(float v, const MassRef& r) {
   return f2ull_rn(mass_f32(v, r) * kMassScaleF);
