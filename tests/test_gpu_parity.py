@@ -248,3 +248,30 @@ def test_top_p_cut_among_signed_zeros(tk, monkeypatch, dtype):
         monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
         out = _run_apply(tk, x, dtype, p, None)
         _check_all(out, x, dtype, p, None, f"{dtype} signed zeros plan={plan!r}")
+
+
+@pytest.mark.parametrize("dtype", DTS)
+def test_sampled_bound_too_high_restarts(tk, dtype):
+    """Rows whose first load groups (the sample that bounds top-k candidates
+    in a single pass) hold one large value per vector and the rest of the
+    row nothing comparable: the sampled bound then has fewer than k elements
+    above it, and the row must restart with the exact two-pass bound."""
+    rng = np.random.default_rng(29)
+    B, V = 2, 131072
+    x = rng.standard_normal((B, V)).astype(np.float32)
+    per_warp = V // 8 // 16                     # 16-byte vectors per warp (16-bit rows)
+    if dtype == "f32":
+        per_warp = V // 4 // 16
+    vec = 8 if dtype != "f32" else 4
+    big = 10.0 + 0.25 * np.arange(16 * 128, dtype=np.float32)
+    rng.shuffle(big)
+    i = 0
+    for w in range(16):
+        for t in range(128):                    # the first 128 vectors of warp w
+            x[:, (w * per_warp + t) * vec] = big[i]
+            i += 1
+    xr = np.stack([to_raw(r, dtype) for r in x])
+    k = np.array([1000, 1300], dtype=np.int32)
+    for p in (None, to_raw([0.9, 0.5], dtype)):
+        out = _run_apply(tk, xr, dtype, p, k)
+        _check_all(out, xr, dtype, p, k, f"{dtype} sampled bound restart p={p is not None}")

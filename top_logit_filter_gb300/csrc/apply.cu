@@ -633,13 +633,17 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       }
     }
   };
-  // Top-k with small k: the first load group of every warp bounds the
-  // candidates (k of its vectors reach the bucket floor of their k-th
-  // largest maximum), so pass A collects them and the row is read once,
-  // when the expected number of candidates fits the lists comfortably.
+  // Top-k: the first load group of every warp (fv vectors, a sample of the
+  // row) bounds the candidates.  L is the bucket floor of the rk-th largest
+  // vector maximum of the sample, rk = 2k x (sample share of the row), at
+  // least 8: the row then holds about 2k elements >= L (rarely fewer than
+  // k), which pass A lists, so the row is read once.  With rk = k (the sample is most of the row) L is a bound
+  // by construction; otherwise it is checked after the pass: fewer than k
+  // listed elements, or lists that overflow, restart the two-pass flow.
   const int fv = min(nvec, kWarps * 32 * kLoadsHeavy);
-  const bool single = topk && !generic_only && kv <= fv &&
-                      4LL * kv * V <= (long long)fv * VEC * kWarps * CAPW;
+  const long long rk_want = (2LL * kv * fv * VEC + V - 1) / V;
+  const int rk = (int)min((long long)kv, max(8LL, rk_want));
+  const bool single = topk && !generic_only && rk <= fv && 8LL * kv <= (long long)kWarps * CAPW;
   uint32_t Lkey = 0;  // candidate bound (candidate path)
 
   // ---- pass A (from HBM): the row max, plus the 12-bit first-digit
@@ -659,8 +663,8 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
           __syncthreads();
           const int lb = select_desc_f<kBins / kThreads>(
               [&](int j) -> unsigned long long { return hist[swz<kBPT>(kBPT * tid + j)]; },
-              (unsigned long long)kv, h).bin;
-          // fewer than k vectors in the groups: every element (the lists overflow)
+              (unsigned long long)rk, h).bin;
+          // fewer than rk vectors in the groups: every element (the lists overflow)
           Lkey = lb > 0 ? (uint32_t)lb << SHB : order_key<DT>(D::kNegInf) + 1u;
           L2 = P::splat((uint32_t)raw_of_key<DT>(Lkey));
         },
@@ -818,10 +822,13 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         h.over = 1;
       }
       __syncthreads();
-      listed = !h.over;
+      unsigned long long nl = 0;  // listed elements
+      for (int w = 0; w < kWarps; ++w) nl += h.nseg[w];
+      listed = !h.over && nl >= (unsigned long long)kv;
       if (!listed) {
-        // the bound from the first load groups was too loose: start over
-        // from the whole row's vector maxima
+        // the bound from the first load groups was too loose (or, fewer
+        // than k listed, above the k-th largest): start over from the
+        // whole row's vector maxima
         __syncthreads();
         for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
         if (tid < kWarps) h.nseg[tid] = 0;
