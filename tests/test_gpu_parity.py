@@ -275,3 +275,28 @@ def test_sampled_bound_too_high_restarts(tk, dtype):
     for p in (None, to_raw([0.9, 0.5], dtype)):
         out = _run_apply(tk, xr, dtype, p, k)
         _check_all(out, xr, dtype, p, k, f"{dtype} sampled bound restart p={p is not None}")
+
+
+def _two_cluster_rows(dtype):
+    """fp16/bf16 rows with a cluster of values near -2 and one near +3 (and
+    nothing between), sized so that the mass below the gap is close to
+    1 - p: the rigorous window of the top-p cut then reaches from one
+    cluster across zero to the other, over a thousand empty buckets."""
+    rng = np.random.default_rng(41)
+    V = 8192
+    rows = []
+    for ratio in np.linspace(2.10, 2.55, 16):
+        n2 = int(round((V - 1) / (1 + ratio)))
+        n1 = V - 1 - n2
+        v = np.concatenate([rng.uniform(-2.0, -1.9, n1), rng.uniform(2.9, 3.0, n2), [3.0]]).astype(np.float32)
+        rows.append(rng.permutation(v))
+    x = np.stack([to_raw(r, dtype) for r in rows])
+    p = to_raw(np.full(len(rows), 1.0 - 1.0 / 64.0, dtype=np.float32), dtype)
+    return x, p
+
+
+@pytest.mark.parametrize("dtype", ("f16", "bf16"))
+def test_top_p_window_across_empty_buckets(tk, dtype):
+    x, p = _two_cluster_rows(dtype)
+    out = _run_apply(tk, x, dtype, p, None)
+    _check_all(out, x, dtype, p, None, f"{dtype} two clusters")

@@ -1104,11 +1104,15 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     // the window), else only the occupied ones (a window that crosses zero
     // spans thousands of nearly empty buckets)
     const bool direct = w1 >= w0 && (w1 - w0 + 1) <= kKeyBlocks;
-    uint32_t occ = 0;
+    // which of this thread's buckets get counters, decided before block_of
+    // (which shares the counts' words) overwrites the counts
+    uint32_t occ = 0, takes = 0;
 #pragma unroll
     for (int j = 0; j < BPT; ++j) {
       const int b = BPT * tid + j;
-      occ += (b >= w0 && b <= w1 && (direct || hist[swz<kBPT>(b)] != 0)) ? 1u : 0u;
+      const bool t = b >= w0 && b <= w1 && (direct || hist[swz<kBPT>(b)] != 0);
+      takes |= (t ? 1u : 0u) << j;
+      occ += t ? 1u : 0u;
     }
     unsigned long long nocc;
     uint32_t id = (uint32_t)block_exclusive_scan(occ, &nocc, h.ws);
@@ -1116,7 +1120,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
 #pragma unroll
       for (int j = 0; j < BPT; ++j) {
         const int b = BPT * tid + j;
-        if (b >= w0 && b <= w1 && (direct || hist[swz<kBPT>(b)] != 0)) {
+        if ((takes >> j) & 1u) {
           bucket_of[id] = (uint16_t)b;
           block_of[b] = id++;
         } else {
