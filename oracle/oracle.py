@@ -230,3 +230,117 @@ def apply_sorted(sv_raw, si, dtype, p_raw=None, k=None, rows=None):
         kb = None if k is None else int(k[b])
         out[b], infos[b] = apply_sorted_row(sv_raw[b], si[b], dtype, pb, kb)
     return out, infos
+
+
+# ------------------------------------------ post-filter stage: min-p and sampling
+# "[V2]" is the page "aclnnTopKTopPSampleV2" (CANN community edition API
+# reference), cited by its headings: "Formula / minP sampling" and
+# "Formula / Subsequent processing" (its None and QSample modes), plus
+# "Constraints".  That operator runs top-k, top-p, min-p and the sample in
+# one call on a sorted row; this stage takes the filter's output instead
+# (original order, masked elements -inf) and applies the last two steps.
+#
+# Readings (listed again in the design notes):
+#   S1  The probabilities are the softmax over the filter's survivors.  [V2]
+#       forms them over the top-k survivors before the top-p mask; min-p
+#       (probs < max_prob * minP) and the sample (argmax of probs / (q +
+#       eps)) compare ratios of probabilities, in which the normaliser
+#       cancels, so the choice of normaliser changes no decision.
+#   S2  minP <= 0 skips min-p; minP >= 1 keeps the one element of largest
+#       value ([V2] Formula / minP sampling, "in other cases"); among equal
+#       largest values, the one that comes last in the stable ascending order
+#       (the largest index) -- the position the top-p step never masks.
+#   S3  q is one fp32 variate per element in original index order ([V2]
+#       Constraints: q has the logits' shape); [V2] indexes it by sorted
+#       position, which this stage does not have.
+#   S4  ArgMax ties go to the element that comes last in the stable
+#       ascending order (the largest index among equal values), so that
+#       the None mode returns the element the filter always keeps.
+#   S5  eps is not given a value by [V2]; it is an argument here.
+#   S6  Probabilities, thresholds and ratios are formed in fp64 from the
+#       exactly decoded inputs (q and eps as fp32 values).
+
+
+class SampleInfo:
+    """Per-row intermediates of the sample stage, for the tests' tolerances."""
+
+    __slots__ = ("alive", "e", "keep", "ratio", "min_p", "last")
+
+    def __init__(self, alive, e, keep, ratio, min_p, last):
+        self.alive, self.e, self.keep, self.ratio, self.min_p, self.last = alive, e, keep, ratio, min_p, last
+
+
+def survivor_probs(vals: np.ndarray):
+    """Softmax over the filter's survivors (S1).  Returns (alive, last, e,
+    probs): alive marks the elements that are not -inf, last is the index
+    of the largest value that comes last in the stable ascending order (S2,
+    S4), e = exp(x - max) and probs = e / sum(e), both fp64."""
+    alive = vals != -np.inf
+    m = vals[alive].max()
+    last = int(np.flatnonzero(alive & (vals == m))[-1])
+    e = np.where(alive, np.exp(np.where(alive, vals - m, 0.0)), 0.0)
+    return alive, last, e, e / e.sum()
+
+
+def min_p_keep(alive: np.ndarray, probs: np.ndarray, last: int, mp):
+    """[V2] Formula / minP sampling: minPThd = max(probs) * minP, and
+    elements with probs < minPThd are removed; minP <= 0 skips the step and
+    minP >= 1 keeps the largest element alone (S2)."""
+    if mp is None or not (mp > 0.0):
+        return alive.copy()
+    if mp >= 1.0:
+        keep = np.zeros(alive.shape[0], dtype=bool)
+        keep[last] = True
+        return keep
+    thd = probs[last] * mp
+    return alive & ~(probs < thd)
+
+
+def sample_token(probs: np.ndarray, keep: np.ndarray, last: int, q, eps: float):
+    """[V2] Formula / Subsequent processing.  None mode (q None): ArgMax of
+    the probabilities, i.e. the largest element (S4).  QSample mode: ArgMax of
+    probs / (q + eps) over the kept elements, ties to the largest index.
+    Returns (token, ratio)."""
+    if q is None:
+        return last, None
+    qv = np.asarray(q, dtype=np.float32).astype(np.float64)
+    ratio = np.where(keep, probs / (qv + float(np.float32(eps))), -np.inf)
+    return int(np.flatnonzero(ratio == ratio.max())[-1]), ratio
+
+
+def sample_row(f_raw: np.ndarray, dtype: str, min_p=None, q=None, eps: float = 1e-10):
+    """Min-p and the sample on one filtered row (readings S1-S6).
+
+    Returns (out_raw, token, SampleInfo).  out_raw is the row with the
+    elements that min-p removes set to -inf; token is the original index
+    chosen by ArgMax of the probabilities (q None, [V2] Subsequent
+    processing / None) or of probs / (q + eps) (QSample).  A row without a
+    finite element (outside the filter's contract) is returned unchanged
+    with token -1."""
+    V = int(f_raw.shape[0])
+    bits = raw_bits(f_raw, dtype)
+    vals = decode(f_raw, dtype)
+    if not (vals != -np.inf).any():
+        return _bits_to_raw(bits.copy(), dtype), -1, SampleInfo(vals != -np.inf, np.zeros(V), vals != -np.inf,
+                                                                None, None, -1)
+    alive, last, e, probs = survivor_probs(vals)
+    mp = None if min_p is None else float(np.float32(min_p))
+    keep = min_p_keep(alive, probs, last, mp)
+    out_bits = np.where(keep, bits, neg_inf_bits(dtype)).astype(bits.dtype)
+    token, ratio = sample_token(probs, keep, last, q, eps)
+    return _bits_to_raw(out_bits, dtype), token, SampleInfo(alive, e, keep, ratio, mp, last)
+
+
+def sample(f_raw, dtype, min_p=None, q=None, eps: float = 1e-10, rows=None):
+    """Batched sample stage over [B, V]; min_p is [B] fp32 or None, q is
+    [B, V] fp32 or None.  Returns (out_raw, tokens, {row: SampleInfo})."""
+    f_raw = np.asarray(f_raw)
+    B = f_raw.shape[0]
+    out = np.zeros_like(f_raw)
+    tokens = np.full(B, -1, dtype=np.int64)
+    infos = {}
+    for b in (range(B) if rows is None else rows):
+        mp = None if min_p is None else min_p[b]
+        qb = None if q is None else q[b]
+        out[b], tokens[b], infos[b] = sample_row(f_raw[b], dtype, mp, qb, eps)
+    return out, tokens, infos
