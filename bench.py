@@ -300,12 +300,96 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def run_sample(args):
+    """The post-filter stage on the filter's output of the same batch: one
+    topkp_sample call per step (min-p, QSample with Exp(1) variates, the
+    output row), after the same L2 flush.  One JSON line."""
+    import numpy as np
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import top_logit_filter_gb300 as tk
+    from rawutil import raw_to_torch
+    from top_logit_filter_gb300 import workloads
+
+    w = workloads.make(WORKLOAD)
+    B, V, dt = w["B"], w["V"], w["dtype"]
+    x = raw_to_torch(w["x"], dt, dev)
+    f = tk.apply(x, p=raw_to_torch(w["p"], dt, dev), k=torch.from_numpy(w["k"]).to(dev))
+    rng = np.random.default_rng(SAMPLE_SEED)
+    q = torch.from_numpy(rng.exponential(1.0, size=(B, V)).astype(np.float32)).to(dev)
+    mp = torch.from_numpy(rng.uniform(0.001, 0.2, size=B).astype(np.float32)).to(dev)
+    out = torch.empty_like(f)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        tok, _ = tk.sample(f, min_p=mp, q=q, out=out)
+    torch.cuda.synchronize(dev)
+    kept = int((out.view(torch.int16) != -128).sum().item())   # bf16 -inf is 0xFF80
+
+    def timed(call, prep=None):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            if prep is not None:
+                prep()
+            flush.zero_()
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        return sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
+
+    with ClockSampler(0) as clocks:
+        total_s = timed(lambda: tk.sample(f, min_p=mp, q=q, out=out))
+    # the same stage writing only what min-p removes (in place on a copy of
+    # the filter's output, restored before the flush of every step), and the
+    # token alone
+    f2 = f.clone()
+    in_place_s = timed(lambda: tk.sample(f2, min_p=mp, q=q, out=f2), prep=lambda: f2.copy_(f))
+    token_s = timed(lambda: tk.sample(f, min_p=mp, q=q, want_out=False))
+    tk.device_status(dev)
+    alg_bytes = B * V * 2 * 2 + 4 * kept
+    kernel_s = total_s / args.steps
+    peak, peak_kind = _peak_hbm()
+    achieved = alg_bytes / kernel_s / 1e9
+    line = {
+        "metric": "rows/s and achieved HBM GB/s, post-filter stage (min-p + exponential-race sample), "
+                  "B=256 V=128256 bf16",
+        "value": B * args.steps / total_s, "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * kernel_s, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "sample_after_apply_joint_B256_V128256_bf16", "B": B, "V": V,
+                   "input": "the filter's output of the joint top-k + top-p batch; min_p ~ U[0.001, 0.2]; "
+                            "q ~ Exp(1) fp32",
+                   "kept_after_min_p": kept,
+                   "ms_per_step_in_place": 1e3 * in_place_s / args.steps,
+                   "ms_per_step_token_only": 1e3 * token_s / args.steps,
+                   "l2": "flushed before every timed step (512 MiB memset, outside the events)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "peak_source": f"{peak_kind} (copy bandwidth, burst)",
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+SAMPLE_SEED = 4242
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--op", choices=("filter", "sample"), default="filter",
+                    help="filter: the headline topkp_apply step; sample: the post-filter stage alone")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing (profiling runs)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work for cpu_baseline")
     args = ap.parse_args()
@@ -313,6 +397,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "sample":
+        run_sample(args)
     else:
         run_ours(args)
 

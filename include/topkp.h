@@ -132,6 +132,53 @@ topkp_status topkp_apply_sorted(const void* sorted_value, const int32_t* sorted_
                                 const void* p, const int32_t* k, const void* logits,
                                 void* out, void* stream);
 
+/*
+ * topkp_sample -- the last two steps of the web page "aclnnTopKTopPSampleV2"
+ * (CANN API reference; Formula / minP sampling and Formula / Subsequent
+ * processing, its None and QSample modes), run on the output of
+ * topkp_apply or topkp_apply_sorted: original order, filtered elements -inf.
+ * Per row, with probs the softmax over the elements that are not -inf:
+ *   1. min-p (min_p != NULL and min_p[b] > 0): every element whose
+ *      probability is below min_p[b] times the largest probability becomes
+ *      -inf; with min_p[b] >= 1 only the largest element stays (of equal
+ *      largest values, the one with the largest index);
+ *   2. the token: with q == NULL, the index of the largest element (ties:
+ *      the largest index); otherwise the index of the largest
+ *      probs / (q + eps) among the elements step 1 kept (ties: the largest
+ *      index).  With q drawn i.i.d. from Exp(1), that index is a draw from
+ *      probs.
+ * The page forms probs over the top-k survivors and indexes q by sorted
+ * position; here probs are over the filter's survivors and q follows the
+ * original order.  Both decisions compare ratios of probabilities, so the
+ * normaliser changes none of them.
+ *
+ *   filtered  device, [B, V] of dtype, row stride ld elements (>= V).  A row
+ *             must hold at least one element that is not -inf; a row without
+ *             one is copied unchanged and gets token -1.
+ *   B, V      rows and row length (>= 0); B == 0 or V == 0 returns
+ *             TOPKP_SUCCESS without a launch.
+ *   dtype     TOPKP_F32, TOPKP_F16 or TOPKP_BF16.
+ *   min_p     device, [B] float, or NULL (step 1 off).
+ *   q         device, [B, V] float, row stride ldq (>= V), or NULL (None
+ *             mode).  Values are expected >= 0.
+ *   eps       added to every q (the page names it without a value), >= 0.
+ *   out       device, [B, V] of dtype, row stride ld_out (>= V), or NULL:
+ *             the rows after step 1 (input bits or -inf).  out == filtered
+ *             with ld_out == ld is allowed; other overlaps are rejected.
+ *   token     device, [B] int32, or NULL.  out and token must not both be
+ *             NULL.
+ *   stream    cudaStream_t to launch on.
+ * Results.  The kernel compares base-2 logarithms of the ratios in fp32
+ * ((x - max) log2 e against log2(min_p[b]); (x - max) log2 e - log2(q + eps)
+ * for the race), so a min-p decision can differ from exact arithmetic only
+ * where exp(x - max) lies within about 1e-5 (relative) of min_p[b], and the
+ * token only where another kept element's probs / (q + eps) lies within
+ * about 1e-5 (relative) of the largest.  Deterministic.
+ */
+topkp_status topkp_sample(const void* filtered, int64_t B, int64_t V, int64_t ld, topkp_dtype dtype,
+                          const float* min_p, const float* q, int64_t ldq, float eps,
+                          void* out, int64_t ld_out, int32_t* token, void* stream);
+
 /* One-line description of the last non-zero status returned on the calling
  * thread ("" if none).  The pointer stays valid until the thread's next call
  * into the library. */
@@ -143,7 +190,8 @@ const char* topkp_last_error_string(void);
 topkp_status topkp_device_status(void* stream);
 
 /* Number of kernel launches the most recent successful topkp_apply /
- * topkp_apply_sorted call on this thread enqueued (0 for an empty problem). */
+ * topkp_apply_sorted / topkp_sample call on this thread enqueued (0 for an
+ * empty problem). */
 int topkp_last_launch_count(void);
 
 #ifdef __cplusplus

@@ -26,7 +26,7 @@ def _declared():
 
 
 def test_header_declares_the_expected_calls():
-    assert _declared() == sorted(["topkp_apply", "topkp_apply_sorted", "topkp_last_error_string",
+    assert _declared() == sorted(["topkp_apply", "topkp_apply_sorted", "topkp_sample", "topkp_last_error_string",
                                   "topkp_device_status", "topkp_last_launch_count"])
 
 
@@ -89,6 +89,27 @@ def test_sorted_argument_errors(lib):
     assert call(B=0) == 0
 
 
+def test_sample_argument_errors(lib):
+    def call(x=FAKE, B=2, V=8, ld=8, dt=BF16, mp=None, q=FAKE + 4096, ldq=8, eps=1e-10, out=FAKE + 8192, ldo=8,
+             tok=FAKE + 12288):
+        return lib.topkp_sample(x, B, V, ld, dt, mp, q, ldq, eps, out, ldo, tok, None)
+    assert call(out=None, tok=None) == NULLPTR
+    assert call(x=None) == NULLPTR
+    assert call(dt=5) == INVALID
+    assert call(B=-1) == INVALID
+    assert call(ld=7) == INVALID
+    assert call(ldq=4) == INVALID
+    assert call(ldo=2) == INVALID
+    assert call(eps=-1.0) == INVALID
+    assert call(tok=FAKE + 12289) == INVALID          # token not 4-byte aligned
+    assert call(out=FAKE + 8) == INVALID              # out partially overlaps filtered
+    assert call(out=FAKE + 4096 + 16) == INVALID      # out overlaps q
+    assert call(tok=FAKE + 4) == INVALID              # token overlaps filtered
+    assert call(B=0) == 0
+    assert call(V=0, x=None) == 0
+    assert lib.topkp_last_launch_count() == 0
+
+
 def test_no_device_fails_loudly_instead_of_falling_back(lib):
     """Valid arguments but no usable GPU: the call must report a launch error
     (there is no CPU path)."""
@@ -97,6 +118,7 @@ def test_no_device_fails_loudly_instead_of_falling_back(lib):
         pytest.skip("a GPU is present")
     assert _apply(lib) == LAUNCH
     assert b"device" in lib.topkp_last_error_string()
+    assert lib.topkp_sample(FAKE, 2, 8, 8, BF16, None, None, 8, 1e-10, None, 8, FAKE + 8192, None) == LAUNCH
 
 
 def test_python_binding_rejects_cpu_tensors():

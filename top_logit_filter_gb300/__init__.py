@@ -7,12 +7,15 @@ the calls raise.
 
     out = apply(logits, p=None, k=None, out=None)
     out = apply_sorted(sorted_value, sorted_indices, p=None, k=None, logits=None, out=None)
+    token, out = sample(filtered, min_p=None, q=None, eps=1e-10, out=None, want_out=True)
 
 Semantics: section 2 of the web page "CANN ops-nn 算子实战：
 ApplyTopKTopPWithSorted 的 top-k/top-p 采样过滤原理与 aclnn 调用指南" --
 per row, values strictly below the k-th largest become -inf, then sorted
 positions whose fp32 cumulative softmax probability is <= 1-p become -inf
-(never the largest), and every other element keeps its bits.
+(never the largest), and every other element keeps its bits.  ``sample``
+runs the min-p step and the sample of the page "aclnnTopKTopPSampleV2" on
+such filtered rows.
 """
 from __future__ import annotations
 
@@ -130,6 +133,44 @@ def apply_sorted(sorted_value, sorted_indices, p=None, k=None, logits=None, out=
         _check(lib.topkp_apply_sorted(_ptr(sorted_value), _ptr(sorted_indices), B, V, dt, _ptr(p), _ptr(k),
                                       _ptr(logits), _ptr(out), _stream(dev)))
     return out
+
+
+def sample(filtered, min_p=None, q=None, eps: float = 1e-10, out=None, want_out: bool = True):
+    """Min-p and the exponential-race sample on filtered rows (topkp_sample).
+
+    filtered: [B, V] CUDA tensor (the output of ``apply`` / ``apply_sorted``:
+    logits or -inf).  min_p: [B] float32 (or None).  q: [B, V] float32
+    variates, e.g. drawn from Exp(1), or None for ArgMax.  Returns
+    (token, out): token is a [B] int32 tensor of original indices; out holds
+    the rows after min-p (``filtered`` itself may be passed as out), or None
+    when ``want_out`` is false."""
+    torch = _torch()
+    lib = _lib.load()
+    if not torch.is_tensor(filtered) or filtered.dim() != 2 or not filtered.is_cuda:
+        raise ValueError("filtered must be a 2-D CUDA tensor")
+    dt = _dtype_code(filtered)
+    if filtered.stride(1) != 1:
+        filtered = filtered.contiguous()
+    B, V = filtered.shape
+    dev = filtered.device
+    min_p = _vec(min_p, B, torch.float32, "min_p", dev)
+    if q is not None:
+        if not torch.is_tensor(q) or q.shape != (B, V) or q.dtype != torch.float32 or q.device != dev:
+            raise ValueError("q must be a float32 tensor shaped like filtered on the same device")
+        if q.stride(1) != 1:
+            q = q.contiguous()
+    if want_out and out is None:
+        out = torch.empty((B, V), dtype=filtered.dtype, device=dev)
+    if out is not None and (out.shape != (B, V) or out.dtype != filtered.dtype or out.device != dev
+                            or out.stride(1) != 1):
+        raise ValueError("out must match filtered in shape, dtype and device, with stride(1) == 1")
+    token = torch.empty(B, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.topkp_sample(_ptr(filtered), B, V, filtered.stride(0) if B > 1 else V, dt, _ptr(min_p),
+                                _ptr(q), (q.stride(0) if B > 1 else V) if q is not None else V, float(eps),
+                                _ptr(out), (out.stride(0) if B > 1 else V) if out is not None else V,
+                                _ptr(token), _stream(dev)))
+    return token, out
 
 
 def device_status(device=None) -> None:

@@ -232,6 +232,72 @@ topkp_status topkp_apply_sorted(const void* sorted_value, const int32_t* sorted_
   return TOPKP_SUCCESS;
 }
 
+topkp_status topkp_sample(const void* filtered, int64_t B, int64_t V, int64_t ld, topkp_dtype dtype,
+                          const float* min_p, const float* q, int64_t ldq, float eps,
+                          void* out, int64_t ld_out, int32_t* token, void* stream) {
+  g_last_launches = 0;
+  if (!out && !token) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_sample: out and token are both NULL");
+  const int es = esize_of(dtype);
+  if (!es) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample: unknown dtype %d", (int)dtype);
+  if (B < 0 || V < 0) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample: negative shape B=%lld V=%lld", (long long)B, (long long)V);
+  if (V > TOPKP_MAX_V)
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample: V=%lld exceeds the maximum %lld", (long long)V, (long long)TOPKP_MAX_V);
+  if (B == 0 || V == 0) return TOPKP_SUCCESS;
+  if (!filtered) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_sample: filtered is NULL");
+  if (ld < V || (out && ld_out < V) || (q && ldq < V))
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample: row stride below V (ld=%lld ld_out=%lld ldq=%lld V=%lld)",
+                (long long)ld, (long long)ld_out, (long long)ldq, (long long)V);
+  if (!(eps >= 0.0f)) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample: eps must be >= 0");
+  if ((uintptr_t)filtered % es || (out && (uintptr_t)out % es) || (min_p && (uintptr_t)min_p % 4) ||
+      (q && (uintptr_t)q % 4) || (token && (uintptr_t)token % 4))
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample: a pointer is not aligned to its element size");
+  const size_t xbytes = (size_t)((B - 1) * ld + V) * es;
+  const size_t obytes = out ? (size_t)((B - 1) * ld_out + V) * es : 0;
+  const size_t qbytes = q ? (size_t)((B - 1) * ldq + V) * 4 : 0;
+  const bool in_place = out == filtered && ld_out == ld;
+  if (out && !in_place && overlaps(filtered, xbytes, out, obytes))
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample: out partially overlaps filtered");
+  if (overlaps(out, obytes, q, qbytes) || overlaps(out, obytes, min_p, (size_t)B * 4) ||
+      overlaps(out, obytes, token, (size_t)B * 4) || overlaps(token, (size_t)B * 4, filtered, xbytes) ||
+      overlaps(token, (size_t)B * 4, q, qbytes) || overlaps(token, (size_t)B * 4, min_p, (size_t)B * 4))
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample: an output overlaps another argument");
+
+  int dev = 0;
+  if (current_sms(&dev) <= 0) return fail(TOPKP_ERR_LAUNCH, "topkp_sample: no usable CUDA device");
+
+  SampleArgs a = {};
+  a.x = filtered;
+  a.out = out;
+  a.min_p = min_p;
+  a.q = q;
+  a.token = token;
+  a.ldx = ld;
+  a.ldo = ld_out;
+  a.ldq = ldq;
+  a.V = (int32_t)V;
+  a.eps = eps;
+  const int64_t max_rows = INT_MAX;
+  int launches = 0;
+  for (int64_t r0 = 0; r0 < B; r0 += max_rows) {
+    const int64_t nb = B - r0 < max_rows ? B - r0 : max_rows;
+    SampleArgs ai = a;
+    ai.B = nb;
+    ai.x = (const char*)filtered + r0 * ld * es;
+    ai.out = out ? (char*)out + r0 * ld_out * es : nullptr;
+    ai.min_p = min_p ? min_p + r0 : nullptr;
+    ai.q = q ? q + r0 * ldq : nullptr;
+    ai.token = token ? token + r0 : nullptr;
+    const cudaError_t e = launch_sample(dtype, ai, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(TOPKP_ERR_LAUNCH, "topkp_sample: launch failed (%s)", cudaGetErrorString(e));
+    }
+    ++launches;
+  }
+  g_last_launches = launches;
+  return TOPKP_SUCCESS;
+}
+
 topkp_status topkp_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) {

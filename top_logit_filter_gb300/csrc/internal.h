@@ -66,6 +66,23 @@ struct SortedPlan {
 SortedPlan plan_sorted(int64_t B, int64_t V, int esize, int num_sms, bool with_logits, const char* force);
 cudaError_t launch_sorted(topkp_dtype dt, const SortedPlan& plan, const SortedArgs& a, cudaStream_t s);
 
+// --------------------------------------------------------------- sample
+// One CTA per filtered row: the largest element (pass 1, from HBM), then
+// min-p and the exponential race over the row again (pass 2, from L2).
+struct SampleArgs {
+  const void* x;           // filtered [B, ldx]
+  void* out;               // [B, ldo] or nullptr
+  const float* min_p;      // [B] or nullptr
+  const float* q;          // [B, ldq] or nullptr
+  int32_t* token;          // [B] or nullptr
+  int64_t ldx, ldo, ldq;
+  int64_t B;
+  int32_t V;
+  float eps;
+};
+
+cudaError_t launch_sample(topkp_dtype dt, const SampleArgs& a, cudaStream_t s);
+
 // The sorted-path translation unit keeps a device error word (bit 0: a
 // bounded wait gave up); this reads and clears it (synchronous).
 cudaError_t sorted_take_device_error(unsigned int* out);

@@ -118,3 +118,23 @@ def presort(xr: np.ndarray, dtype: str):
     idx = np.argsort(keyv, axis=-1, kind="stable")
     sv = np.take_along_axis(xr, idx, axis=-1)
     return np.ascontiguousarray(sv), np.ascontiguousarray(idx.astype(np.int32))
+
+
+def make_filtered(B: int, V: int, dtype: str, seed: int, scale: float = 2.0, empty_rows: int = 0) -> dict:
+    """Inputs of the post-filter stage (min-p and the sample): rows as a
+    filter leaves them.  Logits are scale*N(0,1) cast to dtype; every value
+    below a per-row cut drawn from U[0, 2*scale] becomes -inf (the last
+    ``empty_rows`` rows are all -inf).  min_p is U[0.001, 0.3] per row with
+    10% of rows 0 (min-p off) and 5% at 1.0; q holds Exp(1) variates (fp32).
+    Nothing here computes the stage itself."""
+    rng = np.random.default_rng(seed)
+    x = scale * rng.standard_normal((B, V), dtype=np.float32)
+    cut = rng.uniform(0.0, 2.0 * scale, size=B).astype(np.float32)
+    x = np.where(x >= cut[:, None], x, np.float32(-np.inf)).astype(np.float32)
+    if empty_rows:
+        x[B - empty_rows:] = -np.inf
+    min_p = rng.uniform(0.001, 0.3, size=B).astype(np.float32)
+    min_p[_pick_rows(rng, B, 0.10)] = 0.0
+    min_p[_pick_rows(rng, B, 0.05)] = 1.0
+    q = rng.exponential(1.0, size=(B, V)).astype(np.float32)
+    return dict(B=B, V=V, dtype=dtype, x=cast(x, dtype), min_p=min_p, q=q)
