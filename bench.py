@@ -21,7 +21,6 @@ arm (on rank 0; other ranks exit without work).
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -73,9 +72,12 @@ def _peak_hbm():
 
 
 def _kernel_hash():
+    """Hash of the sources that define the filter kernel (its launch, its
+    device code and the headers both include)."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "top_logit_filter_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
+    csrc = os.path.join(ROOT, "top_logit_filter_gb300", "csrc")
+    for name in ("apply.cu", "common.cuh", "internal.h"):
+        with open(os.path.join(csrc, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
