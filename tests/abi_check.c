@@ -1,0 +1,56 @@
+/* Plain C99 client of include/topkp.h: every entry point links, and the
+ * argument checks answer with the documented status codes before any device
+ * work.  Built and run by tests/test_abi_c.py (no GPU needed). */
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "topkp.h"
+
+static int failures = 0;
+
+static void expect(const char* what, topkp_status got, topkp_status want) {
+  if (got != want) {
+    printf("FAIL %s: status %d, want %d (%s)\n", what, got, want, topkp_last_error_string());
+    ++failures;
+  }
+}
+
+int main(void) {
+  /* never dereferenced: each call below is rejected by its argument checks */
+  void* fake = (void*)(uintptr_t)(1u << 20);
+  const int32_t* fake_k = (const int32_t*)((uintptr_t)(1u << 20) + 4096);
+  void* fake_out = (void*)((uintptr_t)(1u << 20) + 8192);
+  int32_t* fake_tok = (int32_t*)((uintptr_t)(1u << 20) + 12288);
+
+  expect("apply, p and k NULL", topkp_apply(fake, 2, 8, 8, TOPKP_BF16, NULL, NULL, fake_out, 8, NULL),
+         TOPKP_ERR_PARAM_NULLPTR);
+  if (strstr(topkp_last_error_string(), "NULL") == NULL) {
+    printf("FAIL: error string does not name the NULL argument: %s\n", topkp_last_error_string());
+    ++failures;
+  }
+  expect("apply, bad dtype", topkp_apply(fake, 2, 8, 8, (topkp_dtype)9, NULL, fake_k, fake_out, 8, NULL),
+         TOPKP_ERR_PARAM_INVALID);
+  expect("apply, stride below V", topkp_apply(fake, 2, 8, 7, TOPKP_F32, NULL, fake_k, fake_out, 8, NULL),
+         TOPKP_ERR_PARAM_INVALID);
+  expect("apply, empty batch", topkp_apply(fake, 0, 8, 8, TOPKP_F16, NULL, fake_k, fake_out, 8, NULL),
+         TOPKP_SUCCESS);
+  expect("apply_sorted, NULL indices",
+         topkp_apply_sorted(fake, NULL, 2, 8, TOPKP_BF16, NULL, fake_k, NULL, fake_out, NULL),
+         TOPKP_ERR_PARAM_NULLPTR);
+  expect("sample, no output",
+         topkp_sample(fake, 2, 8, 8, TOPKP_BF16, NULL, NULL, 8, 1e-10f, NULL, 8, NULL, NULL),
+         TOPKP_ERR_PARAM_NULLPTR);
+  expect("sample, negative eps",
+         topkp_sample(fake, 2, 8, 8, TOPKP_BF16, NULL, NULL, 8, -1.0f, NULL, 8, fake_tok, NULL),
+         TOPKP_ERR_PARAM_INVALID);
+  expect("sample, empty rows",
+         topkp_sample(fake, 2, 0, 8, TOPKP_BF16, NULL, NULL, 8, 1e-10f, NULL, 8, fake_tok, NULL),
+         TOPKP_SUCCESS);
+  if (topkp_last_launch_count() != 0) {
+    printf("FAIL: launches counted for an empty problem\n");
+    ++failures;
+  }
+  if (failures == 0) printf("abi ok\n");
+  return failures == 0 ? 0 : 1;
+}
