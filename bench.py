@@ -148,17 +148,43 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _cpu_baseline(w, budget_s: float):
-    """The oracle as it stands, one row at a time, for about budget_s seconds."""
+def _cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _cpu_baseline(w, budget_s: float, gpu_out=None):
+    """The oracle as it stands, one row at a time, for about budget_s seconds.
+    When the GPU's output of the same batch is given, the rows the oracle
+    produced are also compared with it (the tests' parity rule)."""
     import oracle as O
     t0 = time.perf_counter()
     rows = 0
+    infos = []
     while rows < w["B"] and (rows < 4 or time.perf_counter() - t0 < budget_s):
-        O.apply_row(w["x"][rows], w["dtype"], w["p"][rows], int(w["k"][rows]))
+        infos.append(O.apply_row(w["x"][rows], w["dtype"], w["p"][rows], int(w["k"][rows]))[1])
         rows += 1
     dt = time.perf_counter() - t0
-    return {"value": rows / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {rows} rows of the B=256 x V=128256 bf16 workload, {dt:.1f} s, single-threaded numpy"}
+    line = {"value": rows / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {rows} rows of the B=256 x V=128256 bf16 workload, {dt:.1f} s, single-threaded numpy",
+            "host": {"cpu": _cpu_model(), "cpu_count": os.cpu_count()}}
+    if gpu_out is not None:
+        from parity import compare_row
+        flips = mismatches = 0
+        for b, info in enumerate(infos):
+            try:
+                flips += compare_row(gpu_out[b], w["x"][b], info, w["dtype"], where=f"bench row {b}")
+            except AssertionError:
+                mismatches += 1
+        line["parity"] = {"rows_checked": rows, "rows_outside_the_bar": mismatches, "top_p_flips_in_band": flips}
+    return line
 
 
 def run_reference(args):
@@ -242,6 +268,8 @@ def run_ours(args):
     tk.device_status(dev)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_s = sum(step_ms) / 1e3
+    q = sorted(step_ms)
+    step_pct = {"p10_us": 1e3 * q[len(q) // 10], "p50_us": 1e3 * q[len(q) // 2], "p90_us": 1e3 * q[(9 * len(q)) // 10]}
     total_s = _max_over_ranks(total_s, ws, dev)
     ms_per_step = 1e3 * total_s / args.steps
     value = _job_rows_per_s(ws, B, args.steps, total_s)
@@ -288,7 +316,7 @@ def run_ours(args):
             "config": {"workload": w["name"], "B": B, "V": V, "mode": "joint top-k + top-p",
                        "l2": "flushed before every timed step (512 MiB memset, outside the events)",
                        "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU",
-                       "wall_s_timed_region": t_wall},
+                       "wall_s_timed_region": t_wall, "step_time": step_pct},
             "achieved_GBps": achieved,
             "roofline": roofline,
             "gpu_launches": args.steps * launches_per_step,
@@ -296,7 +324,8 @@ def run_ours(args):
             "e2e": e2e,
         }
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = _cpu_baseline(w, args.cpu_budget)
+            from rawutil import torch_to_raw
+            line["cpu_baseline"] = _cpu_baseline(w, args.cpu_budget, torch_to_raw(out, dt))
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
