@@ -49,6 +49,7 @@
 #ifndef TOPKP_H
 #define TOPKP_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -179,6 +180,31 @@ topkp_status topkp_sample(const void* filtered, int64_t B, int64_t V, int64_t ld
                           const float* min_p, const float* q, int64_t ldq, float eps,
                           void* out, int64_t ld_out, int32_t* token, void* stream);
 
+/*
+ * topkp_sort -- the sort that aclnnApplyTopKTopP runs before the filter
+ * (section 6.1 of the page: l0op::Sort with descending = false and stable =
+ * true), producing the inputs of topkp_apply_sorted.  Per row:
+ * sorted_value holds the row's elements in ascending order (bits kept, -0
+ * and +0 equal), equal values in increasing original index, and
+ * sorted_indices[b][j] is the column sorted_value[b][j] came from.
+ *
+ *   logits          device, [B, V] of dtype, row stride ld_logits (>= V).
+ *   B, V, dtype     as for topkp_apply; B == 0 or V == 0 returns
+ *                   TOPKP_SUCCESS without a launch.
+ *   sorted_value    device, [B, V] contiguous, dtype.
+ *   sorted_indices  device, [B, V] contiguous int32.
+ *   workspace       device, at least topkp_sort_workspace_size(B, V, dtype)
+ *                   bytes, 256-byte aligned, owned by the caller; its contents
+ *                   on entry do not matter and are clobbered.  The page's
+ *                   two-stage form: ask for the size, then run.
+ *   No output may overlap the logits, another output or the workspace.
+ * Results are exact (a permutation and its values; no arithmetic).
+ */
+size_t topkp_sort_workspace_size(int64_t B, int64_t V, topkp_dtype dtype);
+topkp_status topkp_sort(const void* logits, int64_t B, int64_t V, int64_t ld_logits, topkp_dtype dtype,
+                        void* sorted_value, int32_t* sorted_indices, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
 /* One-line description of the last non-zero status returned on the calling
  * thread ("" if none).  The pointer stays valid until the thread's next call
  * into the library. */
@@ -190,8 +216,8 @@ const char* topkp_last_error_string(void);
 topkp_status topkp_device_status(void* stream);
 
 /* Number of kernel launches the most recent successful topkp_apply /
- * topkp_apply_sorted / topkp_sample call on this thread enqueued (0 for an
- * empty problem). */
+ * topkp_apply_sorted / topkp_sample / topkp_sort call on this thread
+ * enqueued (0 for an empty problem). */
 int topkp_last_launch_count(void);
 
 #ifdef __cplusplus

@@ -26,7 +26,8 @@ def _declared():
 
 
 def test_header_declares_the_expected_calls():
-    assert _declared() == sorted(["topkp_apply", "topkp_apply_sorted", "topkp_sample", "topkp_last_error_string",
+    assert _declared() == sorted(["topkp_apply", "topkp_apply_sorted", "topkp_sample", "topkp_sort",
+                                  "topkp_sort_workspace_size", "topkp_last_error_string",
                                   "topkp_device_status", "topkp_last_launch_count"])
 
 
@@ -108,6 +109,26 @@ def test_sample_argument_errors(lib):
     assert call(B=0) == 0
     assert call(V=0, x=None) == 0
     assert lib.topkp_last_launch_count() == 0
+
+
+def test_sort_workspace_and_argument_errors(lib):
+    ws = lib.topkp_sort_workspace_size(2, 8, BF16)
+    assert ws == 256 + 256                      # 64 B of indices and 32 B of values, each rounded to 256
+    assert lib.topkp_sort_workspace_size(3, 1000, F32) == 12032 + 12032
+    assert lib.topkp_sort_workspace_size(0, 8, BF16) == 0 and lib.topkp_sort_workspace_size(2, 8, 9) == 0
+
+    def call(x=FAKE, B=2, V=8, ld=8, dt=BF16, sv=FAKE + 8192, si=FAKE + 12288, w=FAKE + 16384, wn=512):
+        return lib.topkp_sort(x, B, V, ld, dt, sv, si, w, wn, None)
+    assert call(x=None) == NULLPTR
+    assert call(sv=None) == NULLPTR
+    assert call(w=None) == NULLPTR
+    assert call(dt=4) == INVALID
+    assert call(ld=7) == INVALID
+    assert call(wn=511) == INVALID               # workspace too small
+    assert call(w=FAKE + 16384 + 16) == INVALID  # workspace not 256-byte aligned
+    assert call(sv=FAKE + 4) == INVALID          # overlaps the logits
+    assert call(si=FAKE + 8192 + 8) == INVALID   # overlaps sorted_value
+    assert call(B=0) == 0
 
 
 def test_no_device_fails_loudly_instead_of_falling_back(lib):

@@ -8,6 +8,7 @@ the calls raise.
     out = apply(logits, p=None, k=None, out=None)
     out = apply_sorted(sorted_value, sorted_indices, p=None, k=None, logits=None, out=None)
     token, out = sample(filtered, min_p=None, q=None, eps=1e-10, out=None, want_out=True)
+    sorted_value, sorted_indices = sort(logits)
 
 Semantics: section 2 of the web page "CANN ops-nn 算子实战：
 ApplyTopKTopPWithSorted 的 top-k/top-p 采样过滤原理与 aclnn 调用指南" --
@@ -171,6 +172,40 @@ def sample(filtered, min_p=None, q=None, eps: float = 1e-10, out=None, want_out:
                                 _ptr(out), (out.stride(0) if B > 1 else V) if out is not None else V,
                                 _ptr(token), _stream(dev)))
     return token, out
+
+
+def sort(logits, workspace=None):
+    """The stable ascending sort of every row (topkp_sort): returns
+    (sorted_value, sorted_indices), the inputs of ``apply_sorted``.
+    ``workspace`` is a uint8 CUDA tensor of at least
+    ``sort_workspace_size(B, V, dtype)`` bytes (allocated when None)."""
+    torch = _torch()
+    lib = _lib.load()
+    if not torch.is_tensor(logits) or logits.dim() != 2 or not logits.is_cuda:
+        raise ValueError("logits must be a 2-D CUDA tensor")
+    dt = _dtype_code(logits)
+    if logits.stride(1) != 1:
+        logits = logits.contiguous()
+    B, V = logits.shape
+    dev = logits.device
+    need = int(lib.topkp_sort_workspace_size(B, V, dt))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if workspace.dtype != torch.uint8 or workspace.device != dev or workspace.numel() < need:
+        raise ValueError(f"workspace must be a uint8 tensor of at least {need} bytes on {dev}")
+    sv = torch.empty((B, V), dtype=logits.dtype, device=dev)
+    si = torch.empty((B, V), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.topkp_sort(_ptr(logits), B, V, logits.stride(0) if B > 1 else V, dt, _ptr(sv), _ptr(si),
+                              _ptr(workspace), workspace.numel(), _stream(dev)))
+    return sv, si
+
+
+def sort_workspace_size(B: int, V: int, dtype) -> int:
+    """Bytes of workspace ``sort`` needs for a [B, V] tensor of ``dtype``."""
+    torch = _torch()
+    codes = {torch.float32: _lib.TOPKP_F32, torch.float16: _lib.TOPKP_F16, torch.bfloat16: _lib.TOPKP_BF16}
+    return int(_lib.load().topkp_sort_workspace_size(B, V, codes[dtype]))
 
 
 def device_status(device=None) -> None:

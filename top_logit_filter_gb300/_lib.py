@@ -21,8 +21,8 @@ TOPKP_ERR_DEVICE_TIMEOUT = 561001
 TOPKP_MAX_V = 1 << 23
 
 # every entry point declared in include/topkp.h
-EXPORTS = ("topkp_apply", "topkp_apply_sorted", "topkp_sample", "topkp_last_error_string",
-           "topkp_device_status", "topkp_last_launch_count")
+EXPORTS = ("topkp_apply", "topkp_apply_sorted", "topkp_sample", "topkp_sort", "topkp_sort_workspace_size",
+           "topkp_last_error_string", "topkp_device_status", "topkp_last_launch_count")
 
 _lib = None
 
@@ -42,6 +42,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topkp_apply_sorted.restype = c_int
     lib.topkp_sample.argtypes = [vp, i64, i64, i64, c_int, vp, vp, i64, ctypes.c_float, vp, i64, vp, vp]
     lib.topkp_sample.restype = c_int
+    lib.topkp_sort_workspace_size.argtypes = [i64, i64, c_int]
+    lib.topkp_sort_workspace_size.restype = ctypes.c_size_t
+    lib.topkp_sort.argtypes = [vp, i64, i64, i64, c_int, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.topkp_sort.restype = c_int
     lib.topkp_last_error_string.argtypes = []
     lib.topkp_last_error_string.restype = ctypes.c_char_p
     lib.topkp_device_status.argtypes = [vp]

@@ -298,6 +298,75 @@ topkp_status topkp_sample(const void* filtered, int64_t B, int64_t V, int64_t ld
   return TOPKP_SUCCESS;
 }
 
+size_t topkp_sort_workspace_size(int64_t B, int64_t V, topkp_dtype dtype) {
+  const int es = esize_of(dtype);
+  if (!es || B <= 0 || V <= 0 || V > TOPKP_MAX_V) return 0;
+  // int32 indices first (4-byte aligned), then the values, 256-byte aligned
+  const size_t n = (size_t)B * (size_t)V;
+  return (n * 4 + 255) / 256 * 256 + (n * es + 255) / 256 * 256;
+}
+
+topkp_status topkp_sort(const void* logits, int64_t B, int64_t V, int64_t ld_logits, topkp_dtype dtype,
+                        void* sorted_value, int32_t* sorted_indices, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  g_last_launches = 0;
+  const int es = esize_of(dtype);
+  if (!es) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sort: unknown dtype %d", (int)dtype);
+  if (B < 0 || V < 0) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sort: negative shape B=%lld V=%lld", (long long)B, (long long)V);
+  if (V > TOPKP_MAX_V)
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sort: V=%lld exceeds the maximum %lld", (long long)V, (long long)TOPKP_MAX_V);
+  if (B == 0 || V == 0) return TOPKP_SUCCESS;
+  if (!logits) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_sort: logits is NULL");
+  if (!sorted_value || !sorted_indices) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_sort: an output is NULL");
+  if (!workspace) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_sort: workspace is NULL");
+  if (ld_logits < V)
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sort: row stride %lld below V=%lld", (long long)ld_logits, (long long)V);
+  const size_t need = topkp_sort_workspace_size(B, V, dtype);
+  if (workspace_bytes < need)
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sort: workspace of %zu bytes, %zu needed", workspace_bytes, need);
+  if ((uintptr_t)logits % es || (uintptr_t)sorted_value % es || (uintptr_t)sorted_indices % 4 ||
+      (uintptr_t)workspace % 256)
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sort: a pointer is not aligned (elements; workspace 256 bytes)");
+  const size_t n = (size_t)B * (size_t)V;
+  const size_t xbytes = (size_t)((B - 1) * ld_logits + V) * es;
+  if (overlaps(sorted_value, n * es, logits, xbytes) || overlaps(sorted_indices, n * 4, logits, xbytes) ||
+      overlaps(sorted_value, n * es, sorted_indices, n * 4) || overlaps(workspace, need, logits, xbytes) ||
+      overlaps(workspace, need, sorted_value, n * es) || overlaps(workspace, need, sorted_indices, n * 4))
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sort: outputs, workspace and logits must not overlap");
+
+  int dev = 0;
+  if (current_sms(&dev) <= 0) return fail(TOPKP_ERR_LAUNCH, "topkp_sort: no usable CUDA device");
+
+  SortArgs a = {};
+  a.x = logits;
+  a.sorted_value = sorted_value;
+  a.sorted_indices = sorted_indices;
+  a.ws_index = reinterpret_cast<int32_t*>(workspace);
+  a.ws_value = (char*)workspace + (n * 4 + 255) / 256 * 256;
+  a.ldx = ld_logits;
+  a.V = (int32_t)V;
+  const int64_t max_rows = INT_MAX;
+  int launches = 0;
+  for (int64_t r0 = 0; r0 < B; r0 += max_rows) {
+    const int64_t nb = B - r0 < max_rows ? B - r0 : max_rows;
+    SortArgs ai = a;
+    ai.B = nb;
+    ai.x = (const char*)logits + r0 * ld_logits * es;
+    ai.sorted_value = (char*)sorted_value + r0 * V * es;
+    ai.sorted_indices = sorted_indices + r0 * V;
+    ai.ws_value = (char*)a.ws_value + r0 * V * es;
+    ai.ws_index = a.ws_index + r0 * V;
+    const cudaError_t e = launch_sort(dtype, ai, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(TOPKP_ERR_LAUNCH, "topkp_sort: launch failed (%s)", cudaGetErrorString(e));
+    }
+    ++launches;
+  }
+  g_last_launches = launches;
+  return TOPKP_SUCCESS;
+}
+
 topkp_status topkp_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) {

@@ -83,6 +83,22 @@ struct SampleArgs {
 
 cudaError_t launch_sample(topkp_dtype dt, const SampleArgs& a, cudaStream_t s);
 
+// ----------------------------------------------------------------- sort
+// One CTA per row: a stable least-significant-digit radix sort, 8-bit
+// digits, ping-ponging between the workspace and the outputs.
+struct SortArgs {
+  const void* x;            // logits [B, ldx]
+  void* sorted_value;       // [B, V] contiguous
+  int32_t* sorted_indices;  // [B, V] contiguous
+  void* ws_value;           // [B, V] workspace, dtype
+  int32_t* ws_index;        // [B, V] workspace, int32
+  int64_t ldx;
+  int64_t B;
+  int32_t V;
+};
+
+cudaError_t launch_sort(topkp_dtype dt, const SortArgs& a, cudaStream_t s);
+
 // The sorted-path translation unit keeps a device error word (bit 0: a
 // bounded wait gave up); this reads and clears it (synchronous).
 cudaError_t sorted_take_device_error(unsigned int* out);
