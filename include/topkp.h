@@ -205,6 +205,28 @@ topkp_status topkp_sort(const void* logits, int64_t B, int64_t V, int64_t ld_log
                         void* sorted_value, int32_t* sorted_indices, void* workspace, size_t workspace_bytes,
                         void* stream);
 
+/*
+ * topkp_sort_static -- topkp_sort for callers that cannot allocate device
+ * memory when they sort (they run inside a memory pool they do not own, are
+ * handed only the tensors they work on, or find the GPU's memory already
+ * reserved): the scratch is a fixed 16 MiB array of the library's own device
+ * memory, reserved on every GPU that loads the library until the process
+ * exits.  The source pages have no counterpart to this call.
+ *
+ *   logits, B, V, ld_logits, dtype, sorted_value, sorted_indices, stream
+ *                   as for topkp_sort.
+ *   A problem whose topkp_sort_workspace_size exceeds 16 MiB (for example
+ *   more than 18 rows of V = 152064 bf16) is rejected with
+ *   TOPKP_ERR_PARAM_INVALID and nothing is launched.
+ *   The first call on a device looks up the array's device address (a host
+ *   call that does not touch any stream); make that first call before any
+ *   stream capture.  Every call shares the one array: calls that can overlap
+ *   on the GPU (other streams, other host threads) race on it and must be
+ *   ordered by the caller.  Nothing of an earlier call's scratch is read.
+ */
+topkp_status topkp_sort_static(const void* logits, int64_t B, int64_t V, int64_t ld_logits, topkp_dtype dtype,
+                               void* sorted_value, int32_t* sorted_indices, void* stream);
+
 /* One-line description of the last non-zero status returned on the calling
  * thread ("" if none).  The pointer stays valid until the thread's next call
  * into the library. */

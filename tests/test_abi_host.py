@@ -27,7 +27,7 @@ def _declared():
 
 def test_header_declares_the_expected_calls():
     assert _declared() == sorted(["topkp_apply", "topkp_apply_sorted", "topkp_sample", "topkp_sort",
-                                  "topkp_sort_workspace_size", "topkp_last_error_string",
+                                  "topkp_sort_workspace_size", "topkp_sort_static", "topkp_last_error_string",
                                   "topkp_device_status", "topkp_last_launch_count"])
 
 

@@ -22,7 +22,7 @@ TOPKP_MAX_V = 1 << 23
 
 # every entry point declared in include/topkp.h
 EXPORTS = ("topkp_apply", "topkp_apply_sorted", "topkp_sample", "topkp_sort", "topkp_sort_workspace_size",
-           "topkp_last_error_string", "topkp_device_status", "topkp_last_launch_count")
+           "topkp_sort_static", "topkp_last_error_string", "topkp_device_status", "topkp_last_launch_count")
 
 _lib = None
 
@@ -46,6 +46,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topkp_sort_workspace_size.restype = ctypes.c_size_t
     lib.topkp_sort.argtypes = [vp, i64, i64, i64, c_int, vp, vp, vp, ctypes.c_size_t, vp]
     lib.topkp_sort.restype = c_int
+    lib.topkp_sort_static.argtypes = [vp, i64, i64, i64, c_int, vp, vp, vp]
+    lib.topkp_sort_static.restype = c_int
     lib.topkp_last_error_string.argtypes = []
     lib.topkp_last_error_string.restype = ctypes.c_char_p
     lib.topkp_device_status.argtypes = [vp]

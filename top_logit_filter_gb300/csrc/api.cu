@@ -68,6 +68,14 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s for any single bounded wa
 
 }  // namespace
 
+// For entry points defined in other translation units.
+topkp_status report_error(topkp_status code, const char* msg) {
+  g_last_error = msg;
+  return code;
+}
+void report_launches(int n) { g_last_launches = n; }
+int device_sms(int* dev) { return current_sms(dev); }
+
 // ------------------------------------------------------------------ planners
 static int slice_for(int64_t V, int C) {
   const int64_t s = (V + C - 1) / C;

@@ -99,6 +99,13 @@ struct SortArgs {
 
 cudaError_t launch_sort(topkp_dtype dt, const SortArgs& a, cudaStream_t s);
 
+// Error and launch reporting for entry points outside api.cu (the thread's
+// last error string, the last launch count), and the current device's SM
+// count (-1 without a usable device).
+topkp_status report_error(topkp_status code, const char* msg);
+void report_launches(int n);
+int device_sms(int* dev);
+
 // The sorted-path translation unit keeps a device error word (bit 0: a
 // bounded wait gave up); this reads and clears it (synchronous).
 cudaError_t sorted_take_device_error(unsigned int* out);

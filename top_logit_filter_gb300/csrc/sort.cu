@@ -17,6 +17,9 @@
 //      lands at base + earlier tiles + earlier warps + earlier lanes: a
 //      stable counting sort on the digit.
 // One 512-thread CTA per row; only shared-memory barriers, no waits.
+#include <cstdio>
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -156,3 +159,102 @@ cudaError_t launch_sort(topkp_dtype dt, const SortArgs& a, cudaStream_t s) {
 }
 
 }  // namespace topkp
+
+// ------------------------------------------------- sort without allocation
+// topkp_sort_static: the same sort with its scratch in this library's own
+// device memory.  Some callers cannot allocate device memory at the moment
+// they sort: code that runs inside a memory pool it does not own, a plugin
+// handed only the tensors it works on, or a host that has already reserved
+// the GPU's memory for other work.  For them the scratch lives in one static
+// device array, reserved on every GPU that loads the library and held until
+// the process exits.  Every call uses the same array, so calls that overlap
+// on the GPU (other streams, other host threads) race on it; the sort
+// overwrites all of the scratch it reads, so nothing needs clearing between
+// calls.
+namespace topkp {
+
+constexpr size_t kStaticSortScratch = 16u << 20;  // bytes: the largest workspace this entry point serves
+static __device__ __align__(256) unsigned char g_sort_scratch[kStaticSortScratch];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {};
+}  // namespace
+
+}  // namespace topkp
+
+extern "C" topkp_status topkp_sort_static(const void* logits, int64_t B, int64_t V, int64_t ld_logits,
+                                          topkp_dtype dtype, void* sorted_value, int32_t* sorted_indices,
+                                          void* stream) {
+  using namespace topkp;
+  report_launches(0);
+  char msg[256];
+  const int es = dtype == TOPKP_F32 ? 4 : ((dtype == TOPKP_F16 || dtype == TOPKP_BF16) ? 2 : 0);
+  if (!es) {
+    snprintf(msg, sizeof msg, "topkp_sort_static: unknown dtype %d", (int)dtype);
+    return report_error(TOPKP_ERR_PARAM_INVALID, msg);
+  }
+  if (B < 0 || V < 0 || V > TOPKP_MAX_V) {
+    snprintf(msg, sizeof msg, "topkp_sort_static: bad shape B=%lld V=%lld", (long long)B, (long long)V);
+    return report_error(TOPKP_ERR_PARAM_INVALID, msg);
+  }
+  if (B == 0 || V == 0) return TOPKP_SUCCESS;
+  const size_t need = topkp_sort_workspace_size(B, V, dtype);
+  if (need > kStaticSortScratch) {
+    snprintf(msg, sizeof msg,
+             "topkp_sort_static: B=%lld x V=%lld needs %zu bytes of scratch, above its fixed %zu; use topkp_sort "
+             "with a workspace", (long long)B, (long long)V, need, kStaticSortScratch);
+    return report_error(TOPKP_ERR_PARAM_INVALID, msg);
+  }
+  if (!logits || !sorted_value || !sorted_indices)
+    return report_error(TOPKP_ERR_PARAM_NULLPTR, "topkp_sort_static: logits or an output is NULL");
+  if (ld_logits < V) return report_error(TOPKP_ERR_PARAM_INVALID, "topkp_sort_static: row stride below V");
+  if ((uintptr_t)logits % es || (uintptr_t)sorted_value % es || (uintptr_t)sorted_indices % 4)
+    return report_error(TOPKP_ERR_PARAM_INVALID, "topkp_sort_static: a pointer is not aligned to its element size");
+  const size_t n = (size_t)B * (size_t)V;
+  const uintptr_t x0 = (uintptr_t)logits, x1 = x0 + (size_t)((B - 1) * ld_logits + V) * es;
+  const uintptr_t v0 = (uintptr_t)sorted_value, v1 = v0 + n * es;
+  const uintptr_t i0 = (uintptr_t)sorted_indices, i1 = i0 + n * 4;
+  if ((v0 < x1 && x0 < v1) || (i0 < x1 && x0 < i1) || (v0 < i1 && i0 < v1))
+    return report_error(TOPKP_ERR_PARAM_INVALID, "topkp_sort_static: outputs and logits must not overlap");
+
+  // set-up, once per device, with that device current: the scratch array's
+  // device address (the symbol's host-side name is not one)
+  int dev = -1;
+  if (device_sms(&dev) <= 0 || dev < 0 || dev >= 64)
+    return report_error(TOPKP_ERR_LAUNCH, "topkp_sort_static: no usable CUDA device");
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+      void* p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_sort_scratch);
+      if (e != cudaSuccess || !p) {
+        cudaGetLastError();
+        snprintf(msg, sizeof msg, "topkp_sort_static: cannot find the scratch array on device %d (%s)", dev,
+                 cudaGetErrorString(e));
+        return report_error(TOPKP_ERR_LAUNCH, msg);
+      }
+      g_scratch_addr[dev] = p;
+    }
+    scratch = g_scratch_addr[dev];
+  }
+
+  SortArgs a = {};
+  a.x = logits;
+  a.sorted_value = sorted_value;
+  a.sorted_indices = sorted_indices;
+  a.ws_index = reinterpret_cast<int32_t*>(scratch);
+  a.ws_value = static_cast<char*>(scratch) + (n * 4 + 255) / 256 * 256;
+  a.ldx = ld_logits;
+  a.B = B;  // B * V fits the scratch, so B is far below the grid limit
+  a.V = (int32_t)V;
+  const cudaError_t e = launch_sort(dtype, a, (cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    snprintf(msg, sizeof msg, "topkp_sort_static: launch failed (%s)", cudaGetErrorString(e));
+    return report_error(TOPKP_ERR_LAUNCH, msg);
+  }
+  report_launches(1);
+  return TOPKP_SUCCESS;
+}
