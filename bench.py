@@ -413,14 +413,69 @@ def run_sample(args):
 SAMPLE_SEED = 4242
 
 
+def run_sort(args):
+    """The stable sort (topkp_sort) of the pre-sorted workload's logits
+    (B=512 x V=152064 bf16): one call per step after the same L2 flush, the
+    workspace allocated once outside the timed region.  One JSON line."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import top_logit_filter_gb300 as tk
+    from rawutil import raw_to_torch
+    from top_logit_filter_gb300 import workloads
+
+    w = workloads.make(5)
+    B, V, dt = w["B"], w["V"], w["dtype"]
+    x = raw_to_torch(w["x"], dt, dev)
+    ws = torch.empty(tk.sort_workspace_size(B, V, x.dtype), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        tk.sort(x, workspace=ws)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(0) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            tk.sort(x, workspace=ws)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    total_s = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
+    # bytes a sort must move at least: read the logits, write values and indices
+    alg_bytes = B * V * (2 + 2 + 4)
+    kernel_s = total_s / args.steps
+    peak, peak_kind = _peak_hbm()
+    achieved = alg_bytes / kernel_s / 1e9
+    line = {
+        "metric": "rows/s and achieved HBM GB/s, stable sort of B=512 V=152064 bf16 rows",
+        "value": B * args.steps / total_s, "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * kernel_s, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "sort_B512_V152064_bf16", "B": B, "V": V,
+                   "l2": "flushed before every timed step (512 MiB memset, outside the events)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "peak_source": f"{peak_kind} (copy bandwidth, burst)",
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--op", choices=("filter", "sample"), default="filter",
-                    help="filter: the headline topkp_apply step; sample: the post-filter stage alone")
+    ap.add_argument("--op", choices=("filter", "sample", "sort"), default="filter",
+                    help="filter: the headline topkp_apply step; sample: the post-filter stage alone; "
+                         "sort: the stable sort alone")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing (profiling runs)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work for cpu_baseline")
     args = ap.parse_args()
@@ -430,6 +485,8 @@ def main():
         run_reference(args)
     elif args.op == "sample":
         run_sample(args)
+    elif args.op == "sort":
+        run_sort(args)
     else:
         run_ours(args)
 
