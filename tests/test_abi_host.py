@@ -131,6 +131,21 @@ def test_sort_workspace_and_argument_errors(lib):
     assert call(B=0) == 0
 
 
+def test_sort_static_argument_errors(lib):
+    def call(x=FAKE, B=2, V=8, ld=8, dt=BF16, sv=FAKE + 8192, si=FAKE + 12288):
+        return lib.topkp_sort_static(x, B, V, ld, dt, sv, si, None)
+    assert call(dt=7) == INVALID
+    assert call(B=-1) == INVALID
+    assert call(B=64, V=152064) == INVALID             # needs more than the fixed 16 MiB scratch
+    assert b"scratch" in lib.topkp_last_error_string()
+    assert call(x=None) == NULLPTR
+    assert call(si=None) == NULLPTR
+    assert call(ld=7) == INVALID
+    assert call(sv=FAKE + 4) == INVALID                # overlaps the logits
+    assert call(B=0) == 0 and call(V=0) == 0
+    assert lib.topkp_last_launch_count() == 0
+
+
 def test_no_device_fails_loudly_instead_of_falling_back(lib):
     """Valid arguments but no usable GPU: the call must report a launch error
     (there is no CPU path)."""
@@ -140,6 +155,8 @@ def test_no_device_fails_loudly_instead_of_falling_back(lib):
     assert _apply(lib) == LAUNCH
     assert b"device" in lib.topkp_last_error_string()
     assert lib.topkp_sample(FAKE, 2, 8, 8, BF16, None, None, 8, 1e-10, None, 8, FAKE + 8192, None) == LAUNCH
+    assert lib.topkp_sort(FAKE, 2, 8, 8, BF16, FAKE + 8192, FAKE + 12288, FAKE + 16384, 512, None) == LAUNCH
+    assert lib.topkp_sort_static(FAKE, 2, 8, 8, BF16, FAKE + 8192, FAKE + 12288, None) == LAUNCH
 
 
 def test_python_binding_rejects_cpu_tensors():
