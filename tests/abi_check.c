@@ -47,6 +47,15 @@ int main(void) {
   expect("sample, empty rows",
          topkp_sample(fake, 2, 0, 8, TOPKP_BF16, NULL, NULL, 8, 1e-10f, NULL, 8, fake_tok, NULL),
          TOPKP_SUCCESS);
+  if (topkp_sort_workspace_size(2, 8, TOPKP_BF16) != 512u) {
+    printf("FAIL: sort workspace size for 2 x 8 bf16 is %zu, want 512\n", topkp_sort_workspace_size(2, 8, TOPKP_BF16));
+    ++failures;
+  }
+  expect("sort, workspace too small",
+         topkp_sort(fake, 2, 8, 8, TOPKP_BF16, fake_out, fake_tok, (void*)((uintptr_t)(1u << 20) + 16384), 100, NULL),
+         TOPKP_ERR_PARAM_INVALID);
+  expect("sort_static, above its scratch",
+         topkp_sort_static(fake, 64, 152064, 152064, TOPKP_BF16, fake_out, fake_tok, NULL), TOPKP_ERR_PARAM_INVALID);
   if (topkp_last_launch_count() != 0) {
     printf("FAIL: launches counted for an empty problem\n");
     ++failures;
