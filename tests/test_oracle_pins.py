@@ -205,8 +205,42 @@ def pin_bf16_codec(orc):
     assert orc.decode(np.array([0x3F80, 0xC000, 0x8000], np.uint16), "bf16").tolist() == [1.0, -2.0, -0.0]
 
 
+def pin_topk_survivors(orc, seed=13):
+    """topk_survivors, the helper that tells the parity check a top-k
+    decision (never allowed to differ) from a top-p one, pinned three ways:
+    hand-worked sorted rows; its definition on every k for tiny rows sorted
+    by numpy, not by the oracle (kept iff fewer than k elements are strictly
+    larger); and the RowInfo that apply_row / apply_sorted_row hand to the
+    tests, against the same definition in the stable order."""
+    g = _load("hand_rows.json")["topk_survivors"]
+    for c in g["cases"]:
+        s = np.asarray(to_raw(c["s"], "f32"), dtype=np.float32).astype(np.float64)
+        got = orc.topk_survivors(s, len(s), c["k"])
+        assert np.array_equal(got, np.asarray(c["kept"], dtype=bool)), c
+    rng = np.random.default_rng(seed)
+    for _ in range(200):
+        V = int(rng.integers(1, 9))
+        x = (rng.integers(-3, 4, size=V) * 0.5).astype(np.float64)
+        s = np.sort(x)
+        for k in range(-1, V + 2):
+            want = np.array([(not (1 <= k <= V - 1)) or int((s > s[j]).sum()) < k for j in range(V)])
+            assert np.array_equal(orc.topk_survivors(s, V, k), want), (s, k)
+    for dt in ("f32", "bf16"):
+        V = 61
+        x = to_raw(np.round(rng.standard_normal(V), 0), dt)   # heavy ties
+        xv = orc.decode(x, dt)
+        idx = np.argsort(xv, kind="stable")
+        for k in (1, 2, 5, 30, V - 1, 0, V):
+            for info in (orc.apply_row(x, dt, None, k)[1],
+                         orc.apply_sorted_row(x[idx], idx.astype(np.int32), dt, to_raw([0.5], dt)[0], k)[1]):
+                vals = xv[info.idx]
+                want = np.array([(not (1 <= k <= V - 1)) or int((xv > v).sum()) < k for v in vals])
+                assert np.array_equal(info.topk_kept, want), (dt, k)
+
+
 PINS = [pin_page_example, pin_hand_rows, pin_thresholds, pin_brute_force,
-        pin_topk_partition, pin_invariants, pin_sorted_matches_unsorted, pin_bf16_codec]
+        pin_topk_partition, pin_invariants, pin_sorted_matches_unsorted, pin_bf16_codec,
+        pin_topk_survivors]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -349,9 +383,25 @@ def _mut_cumsum_descending(m):
     m.filter_sorted_row = f
 
 
+def _mut_survivors_off_by_one(m):
+    def f(s, V, k):
+        if not m.topk_enabled(k, V):
+            return np.ones(V, dtype=bool)
+        return ~(s < s[V - int(k) - 1])
+    m.topk_survivors = f
+
+
+def _mut_survivors_le(m):
+    def f(s, V, k):
+        if not m.topk_enabled(k, V):
+            return np.ones(V, dtype=bool)
+        return ~(s <= s[V - int(k)])
+    m.topk_survivors = f
+
+
 MUTANTS = [_mut_topk_le, _mut_topp_lt, _mut_no_last_guard, _mut_softmax_ignores_topk,
            _mut_kth_off_by_one, _mut_ties_reversed, _mut_gather, _mut_thr_unrounded,
-           _mut_cumsum_descending]
+           _mut_cumsum_descending, _mut_survivors_off_by_one, _mut_survivors_le]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=[m.__name__ for m in MUTANTS])
