@@ -72,11 +72,12 @@ def _peak_hbm():
 
 
 def _kernel_hash():
-    """Hash of the sources that define the filter kernel (its launch, its
-    device code and the headers both include)."""
+    """Hash of the sources that define the filter kernel's device code (its
+    own file and the device helpers it includes); declarations of the other
+    kernels do not change it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "top_logit_filter_gb300", "csrc")
-    for name in ("apply.cu", "common.cuh", "internal.h"):
+    for name in ("apply.cu", "common.cuh"):
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -24,9 +24,10 @@
  *
  * Results.  Top-k decisions are exact.  A top-p decision can differ from the
  * exact fp32 definition only at positions whose cumulative probability lies
- * within about 1e-6 of round_D(1 - p) (the library sums probability mass in
- * 64-bit fixed point from fp32 exponentials).  Results are deterministic:
- * the same inputs give the same bits on every call.
+ * within 1e-5 of round_D(1 - p): the library sums probability mass exactly
+ * in 64-bit fixed point, from fp32 exponentials whose relative error is
+ * about 2e-6, and 1e-5 is the bound the tests hold it to.  Results are
+ * deterministic: the same inputs give the same bits on every call.
  *
  * Conventions shared by every entry point.
  *   - All data pointers are DEVICE pointers owned by the caller; the library
@@ -81,6 +82,9 @@ typedef int topkp_status;
  * skipped its writes for the affected rows.  Reported by
  * topkp_device_status(). */
 #define TOPKP_ERR_DEVICE_TIMEOUT 561001
+/* topkp_sort_static only: the device had no room for the library's static
+ * scratch when the sort's module was first loaded on it. */
+#define TOPKP_ERR_NO_MEMORY 561002
 
 /* Largest supported row length: probability mass is summed in unsigned
  * 64-bit fixed point with 2^40 per unit, so a row may hold at most 2^23
@@ -210,19 +214,29 @@ topkp_status topkp_sort(const void* logits, int64_t B, int64_t V, int64_t ld_log
  * memory when they sort (they run inside a memory pool they do not own, are
  * handed only the tensors they work on, or find the GPU's memory already
  * reserved): the scratch is a fixed 16 MiB array of the library's own device
- * memory, reserved on every GPU that loads the library until the process
- * exits.  The source pages have no counterpart to this call.
+ * memory, held until the process exits.  The source pages have no
+ * counterpart to this call.
  *
  *   logits, B, V, ld_logits, dtype, sorted_value, sorted_indices, stream
  *                   as for topkp_sort.
  *   A problem whose topkp_sort_workspace_size exceeds 16 MiB (for example
  *   more than 18 rows of V = 152064 bf16) is rejected with
  *   TOPKP_ERR_PARAM_INVALID and nothing is launched.
- *   The first call on a device looks up the array's device address (a host
- *   call that does not touch any stream); make that first call before any
- *   stream capture.  Every call shares the one array: calls that can overlap
- *   on the GPU (other streams, other host threads) race on it and must be
- *   ordered by the caller.  Nothing of an earlier call's scratch is read.
+ *   When the array is reserved: the sort's code is a module of its own, and
+ *   a GPU reserves the module's 16 MiB when it loads that module.  Under
+ *   CUDA's default lazy module loading that happens at the first
+ *   topkp_sort or topkp_sort_static call on that device, not when the
+ *   library is loaded.  So make one topkp_sort_static call on every device
+ *   you will use before handing the rest of its memory to a pool, and before
+ *   any stream capture: that first call also looks up the array's device
+ *   address (a host call that touches no stream) and keeps it for the
+ *   device.  If the device has no 16 MiB left at that point, the call
+ *   returns TOPKP_ERR_NO_MEMORY and launches nothing.  The kept address
+ *   belongs to the device's context as it was then: after cudaDeviceReset
+ *   this entry point must not be called again in the same process.
+ *   Every call shares the one array: calls that can overlap on the GPU
+ *   (other streams, other host threads) race on it and must be ordered by
+ *   the caller.  Nothing of an earlier call's scratch is read.
  */
 topkp_status topkp_sort_static(const void* logits, int64_t B, int64_t V, int64_t ld_logits, topkp_dtype dtype,
                                void* sorted_value, int32_t* sorted_indices, void* stream);

@@ -10,3 +10,12 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    import flipstats
+    if not flipstats.RECORDS:
+        return
+    terminalreporter.write_sep("-", "tolerated differences per workload (GPU vs oracle)")
+    for name, rows, flips, what in flipstats.RECORDS:
+        terminalreporter.write_line(f"{name}: {rows} rows checked, {flips} {what}")

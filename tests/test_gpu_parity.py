@@ -9,6 +9,7 @@ row where one exists)."""
 import numpy as np
 import pytest
 
+import flipstats
 import oracle as O
 from parity import compare_row
 from rawutil import NEG_INF, bits, raw_to_torch, to_raw, torch_to_raw
@@ -193,7 +194,7 @@ def test_workload_full_size(tk, wl, sample):
         _, info = O.apply_row(w["x"][b], dt, None if w["p"] is None else w["p"][b],
                               None if w["k"] is None else int(w["k"][b]))
         flips += compare_row(out[b], w["x"][b], info, dt, where=f"workload {wl} row {b}")
-    print(f"workload {wl}: {len(rows)} rows checked, {flips} top-p flips inside the band")
+    flipstats.record(f"workload {wl} ({w['name']})", len(rows), flips)
     if wl == 4:
         # top-k alone on every row: out == where(x >= k-th largest, x, -inf)
         xv = O.decode(w["x"], dt)
@@ -219,10 +220,11 @@ def test_workload3_mode_variants_full_size(tk, mode):
                                 k=None if k is None else torch.from_numpy(k).cuda()), dt)
     tk.device_status()
     flips = 0
-    for b in np.random.default_rng(7).choice(w["B"], 40, replace=False):
+    rows = np.random.default_rng(7).choice(w["B"], 40, replace=False)
+    for b in rows:
         _, info = O.apply_row(w["x"][b], dt, None if p is None else p[b], None if k is None else int(k[b]))
         flips += compare_row(out[b], w["x"][b], info, dt, where=f"{mode} row {b}")
-    print(f"{mode}: {flips} top-p flips inside the band")
+    flipstats.record(f"workload 3 as {mode}", len(rows), flips)
 
 
 @pytest.mark.parametrize("dtype", ("f16", "bf16"))

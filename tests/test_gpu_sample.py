@@ -9,6 +9,7 @@ whose probs / (q + eps) is within BAND (relative) of the largest one."""
 import numpy as np
 import pytest
 
+import flipstats
 import oracle as O
 from rawutil import NEG_INF, bits, raw_to_torch, torch_to_raw
 
@@ -170,7 +171,8 @@ def test_sample_full_size_bf16(tk):
     out, tok = _run(tk, d["x"], "bf16", d["min_p"], d["q"])
     flips, tdiff = _check(d["x"], "bf16", d["min_p"], d["q"], out, tok, where="full")
     assert tdiff <= 2, tdiff
-    print(f"full-size sample: {flips} min-p flips, {tdiff} token differences over 256 rows")
+    flipstats.record("sample stage, B=256 x V=128256 bf16 filtered rows", 256, flips, "min-p flips inside the band")
+    flipstats.record("sample stage, B=256 x V=128256 bf16 filtered rows", 256, tdiff, "QSample tokens differing within the band")
 
 
 def test_filter_then_sample_pipeline(tk):

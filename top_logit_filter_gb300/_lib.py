@@ -18,6 +18,7 @@ TOPKP_ERR_PARAM_NULLPTR = 161001
 TOPKP_ERR_PARAM_INVALID = 161002
 TOPKP_ERR_LAUNCH = 561000
 TOPKP_ERR_DEVICE_TIMEOUT = 561001
+TOPKP_ERR_NO_MEMORY = 561002
 TOPKP_MAX_V = 1 << 23
 
 # every entry point declared in include/topkp.h

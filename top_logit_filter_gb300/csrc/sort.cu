@@ -166,8 +166,9 @@ cudaError_t launch_sort(topkp_dtype dt, const SortArgs& a, cudaStream_t s) {
 // they sort: code that runs inside a memory pool it does not own, a plugin
 // handed only the tensors it works on, or a host that has already reserved
 // the GPU's memory for other work.  For them the scratch lives in one static
-// device array, reserved on every GPU that loads the library and held until
-// the process exits.  Every call uses the same array, so calls that overlap
+// device array that a GPU reserves when it loads this file's module (under
+// CUDA's default lazy loading: at the first sort call on that device) and
+// holds until the process exits.  Every call uses the same array, so calls that overlap
 // on the GPU (other streams, other host threads) race on it; the sort
 // overwrites all of the scratch it reads, so nothing needs clearing between
 // calls.
@@ -228,7 +229,16 @@ extern "C" topkp_status topkp_sort_static(const void* logits, int64_t B, int64_t
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (!g_scratch_addr[dev]) {
       void* p = nullptr;
+      // loads this module on the device if it is not loaded yet, which
+      // reserves the array: that can fail for want of memory
       const cudaError_t e = cudaGetSymbolAddress(&p, g_sort_scratch);
+      if (e == cudaErrorMemoryAllocation) {
+        cudaGetLastError();
+        snprintf(msg, sizeof msg,
+                 "topkp_sort_static: device %d is out of memory: loading the sort reserves its %zu-byte static "
+                 "scratch", dev, kStaticSortScratch);
+        return report_error(TOPKP_ERR_NO_MEMORY, msg);
+      }
       if (e != cudaSuccess || !p) {
         cudaGetLastError();
         snprintf(msg, sizeof msg, "topkp_sort_static: cannot find the scratch array on device %d (%s)", dev,
