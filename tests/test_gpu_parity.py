@@ -75,17 +75,24 @@ def _run_apply(tk, x, dtype, p, k, out=None):
     return torch_to_raw(o, dtype)
 
 
-def _check_all(out, x, dtype, p, k, where):
+def _infos(x, dtype, p, k):
+    return [O.apply_row(x[b], dtype, None if p is None else p[b], None if k is None else int(k[b]))[1]
+            for b in range(x.shape[0])]
+
+
+def _check_all(out, x, dtype, p, k, where, infos=None):
     flips = 0
+    infos = _infos(x, dtype, p, k) if infos is None else infos
     for b in range(x.shape[0]):
-        _, info = O.apply_row(x[b], dtype, None if p is None else p[b], None if k is None else int(k[b]))
-        flips += compare_row(out[b], x[b], info, dtype, where=f"{where} row {b}")
+        flips += compare_row(out[b], x[b], infos[b], dtype, where=f"{where} row {b}")
     return flips
 
 
-# TOPKP_FORCE_PLAN: "" = each row takes its own path, "generic" = every row
-# that needs a cut takes the generic radix path.
-PLANS = ["", "generic"]
+# TOPKP_FORCE_PLAN: "" = the planner's choice; "generic" = every row that
+# needs a cut takes the generic radix path; "cN" = every row is split over a
+# cluster of N CTAs (slices may be short or empty), alone or after
+# "generic,".
+PLANS = ["", "generic", "c2", "c8", "generic,c4"]
 
 
 @pytest.mark.parametrize("dtype", DTS)
@@ -97,10 +104,11 @@ def test_small_rows_all_plans(tk, monkeypatch, dtype, V, mode):
     for kind in ("normal", "ties", "zeros", "wide", "logprob", "shifted"):
         x = _rows(rng, B, V, dtype, kind)
         k, p = _kp(rng, B, V, dtype, mode)
+        infos = _infos(x, dtype, p, k)
         for plan in PLANS:
             monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
             out = _run_apply(tk, x, dtype, p, k)
-            _check_all(out, x, dtype, p, k, f"{dtype} V={V} {mode} {kind} plan={plan!r}")
+            _check_all(out, x, dtype, p, k, f"{dtype} V={V} {mode} {kind} plan={plan!r}", infos)
 
 
 @pytest.mark.parametrize("dtype", DTS)
@@ -113,17 +121,20 @@ def test_multi_slice_rows(tk, monkeypatch, dtype):
         x = _rows(rng, B, V, dtype, kind)
         k, p = _kp(rng, B, V, dtype, "kp")
         k[:3] = [0, 37, 900]
-        for plan in PLANS:
+        infos_kp, infos_p = _infos(x, dtype, p, k), _infos(x, dtype, p, None)
+        for plan in PLANS + ["c4"]:
             monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
             out = _run_apply(tk, x, dtype, p, k)
-            _check_all(out, x, dtype, p, k, f"{dtype} {kind} plan={plan!r}")
+            _check_all(out, x, dtype, p, k, f"{dtype} {kind} plan={plan!r}", infos_kp)
             # top-p only (k absent): the mass-table and window paths
             out = _run_apply(tk, x, dtype, p, None)
-            _check_all(out, x, dtype, p, None, f"{dtype} {kind} top-p only plan={plan!r}")
+            _check_all(out, x, dtype, p, None, f"{dtype} {kind} top-p only plan={plan!r}", infos_p)
 
 
+@pytest.mark.parametrize("plan", ["", "c2", "c4"])
 @pytest.mark.parametrize("dtype", DTS)
-def test_strided_unaligned_and_in_place(tk, dtype):
+def test_strided_unaligned_and_in_place(tk, monkeypatch, dtype, plan):
+    monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
     rng = np.random.default_rng(11)
     B, V = 5, 3001
     x = _rows(rng, B, V, dtype, "normal")
@@ -206,6 +217,22 @@ def test_workload_full_size(tk, wl, sample):
             assert np.array_equal(ob[b], exp), f"row {b}"
 
 
+def test_workload3_every_split_full_size(tk, monkeypatch):
+    """All 256 rows of the B=256 x V=128256 bf16 batch against the oracle
+    under every split of a row over a cluster, and the planner's own."""
+    from top_logit_filter_gb300 import workloads
+    w = workloads.make(3)
+    dt = w["dtype"]
+    xt, pt, kt = _workload_inputs(w)
+    infos = _infos(w["x"], dt, w["p"], w["k"])
+    for plan in ("c1", "c2", "c4", "c8", ""):
+        monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
+        out = torch_to_raw(tk.apply(xt, p=pt, k=kt), dt)
+        tk.device_status()
+        flips = _check_all(out, w["x"], dt, w["p"], w["k"], f"workload 3 plan={plan!r}", infos)
+        flipstats.record(f"workload 3 split plan {plan or 'planner'!r}", w["B"], flips)
+
+
 @pytest.mark.parametrize("mode", ["topp_only", "topk_only", "all_rows_joint"])
 def test_workload3_mode_variants_full_size(tk, mode):
     """The B=256 x V=128256 bf16 rows with one filter dropped (or every row
@@ -252,8 +279,9 @@ def test_top_p_cut_among_signed_zeros(tk, monkeypatch, dtype):
         _check_all(out, x, dtype, p, None, f"{dtype} signed zeros plan={plan!r}")
 
 
+@pytest.mark.parametrize("plan", ["", "c2", "c4"])
 @pytest.mark.parametrize("dtype", DTS)
-def test_sampled_bound_too_high_restarts(tk, dtype):
+def test_sampled_bound_too_high_restarts(tk, monkeypatch, dtype, plan):
     """Rows whose first load groups (the sample that bounds top-k candidates
     in a single pass) hold one large value per vector and the rest of the
     row nothing comparable: the sampled bound then has fewer than k elements
@@ -274,6 +302,7 @@ def test_sampled_bound_too_high_restarts(tk, dtype):
             i += 1
     xr = np.stack([to_raw(r, dtype) for r in x])
     k = np.array([1000, 1300], dtype=np.int32)
+    monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
     for p in (None, to_raw([0.9, 0.5], dtype)):
         out = _run_apply(tk, xr, dtype, p, k)
         _check_all(out, xr, dtype, p, k, f"{dtype} sampled bound restart p={p is not None}")
@@ -297,8 +326,10 @@ def _two_cluster_rows(dtype):
     return x, p
 
 
+@pytest.mark.parametrize("plan", ["", "c2", "c8"])
 @pytest.mark.parametrize("dtype", ("f16", "bf16"))
-def test_top_p_window_across_empty_buckets(tk, dtype):
+def test_top_p_window_across_empty_buckets(tk, monkeypatch, dtype, plan):
+    monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
     x, p = _two_cluster_rows(dtype)
     out = _run_apply(tk, x, dtype, p, None)
-    _check_all(out, x, dtype, p, None, f"{dtype} two clusters")
+    _check_all(out, x, dtype, p, None, f"{dtype} two clusters plan={plan!r}")

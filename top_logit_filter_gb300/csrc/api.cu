@@ -77,6 +77,28 @@ void report_launches(int n) { g_last_launches = n; }
 int device_sms(int* dev) { return current_sms(dev); }
 
 // ------------------------------------------------------------------ planners
+int plan_apply(int64_t B, int64_t V, int num_sms, const char* force, int32_t* force_bits) {
+  *force_bits = 0;
+  int cs = 0;
+  if (force && *force) {
+    const char* f = force;
+    if (strncmp(f, "generic", 7) == 0) {
+      *force_bits |= kApplyForceGeneric;
+      f += 7;
+      if (*f == ',') ++f;
+    }
+    if (*f == 'c') cs = atoi(f + 1);
+    if (cs != 1 && cs != 2 && cs != 4 && cs != 8) cs = 0;
+  }
+  if (cs == 0) {
+    // split rows while the split batch still runs as one resident wave (two
+    // CTAs per SM) and each slice keeps kApplyMinSlice elements
+    cs = 1;
+    while (cs < 8 && B * cs * 2 <= 2LL * num_sms && V / (2 * cs) >= kApplyMinSlice) cs *= 2;
+  }
+  return cs;
+}
+
 static int slice_for(int64_t V, int C) {
   const int64_t s = (V + C - 1) / C;
   return (int)((s + 15) / 16 * 16);
@@ -142,8 +164,6 @@ topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_lo
   int dev = 0;
   const int sms = current_sms(&dev);
   if (sms <= 0) return fail(TOPKP_ERR_LAUNCH, "topkp_apply: no usable CUDA device");
-  const char* force = getenv("TOPKP_FORCE_PLAN");
-
   ApplyArgs a = {};
   a.x = logits;
   a.out = out;
@@ -152,9 +172,9 @@ topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_lo
   a.ldx = ld_logits;
   a.ldo = ld_out;
   a.V = (int32_t)V;
-  a.force = (force && strcmp(force, "generic") == 0) ? kApplyForceGeneric : 0;
-  // one CTA per row; grid.x must stay below 2^31
-  const int64_t max_rows = INT_MAX;
+  a.cs = plan_apply(B, V, sms, getenv("TOPKP_FORCE_PLAN"), &a.force);
+  // cs CTAs per row; grid.x must stay below 2^31
+  const int64_t max_rows = INT_MAX / a.cs;
   int launches = 0;
   for (int64_t r0 = 0; r0 < B; r0 += max_rows) {
     const int64_t nb = B - r0 < max_rows ? B - r0 : max_rows;
@@ -167,7 +187,8 @@ topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_lo
     const cudaError_t e = launch_apply(dtype, ai, (cudaStream_t)stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
-      return fail(TOPKP_ERR_LAUNCH, "topkp_apply: launch failed (%s; smem=%zu)", cudaGetErrorString(e), kApplySmem);
+      return fail(TOPKP_ERR_LAUNCH, "topkp_apply: launch failed (%s; cs=%d smem=%zu)", cudaGetErrorString(e), a.cs,
+                  kApplySmem);
     }
     ++launches;
   }

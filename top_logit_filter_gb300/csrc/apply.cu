@@ -59,6 +59,7 @@
 // first r0 then become -inf.
 #include <type_traits>
 
+#include "cluster.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -77,10 +78,11 @@ constexpr int kLoadsSimple = 8;              // vectors in flight per lane, ligh
 constexpr int kLoadsHeavy = 4;               // vectors in flight per lane, per-element work
 
 struct __align__(16) ApplyHdr {
-  unsigned long long ws[2 * kWarps];    // block-scan scratch (paired scans use both halves)
-  unsigned long long sel_off;           // select result: count/mass outside the bin
+  // the small tables come first: cluster merges read them as 16-byte vectors
   unsigned long long small_mass[kSmallBins];
   uint32_t small_cnt[kSmallBins];
+  unsigned long long ws[2 * kWarps];    // block-scan scratch (paired scans use both halves)
+  unsigned long long sel_off;           // select result: count/mass outside the bin
   uint32_t nseg[kWarps];                // candidates in each warp's list
   uint32_t wtie[kWarps];                // ties of T in each warp's sixteenth of the row
   int sel_bin;                          // select result: bin, -1 if none
@@ -94,6 +96,7 @@ struct __align__(16) ApplyHdr {
   int mt_qn;                             // mag clamped to >= floor; qn = bin of the negative floor;
   uint32_t mt_lump;                      // k0 = provisional max key; lump: floors hold zero-equal keys
   uint32_t slot;                         // block_first_true scratch
+  ClSlots cx;                            // cluster exchange slots (rows split over a cluster)
 };
 static_assert(sizeof(ApplyHdr) <= kApplyHdrBytes, "header too large");
 
@@ -405,8 +408,10 @@ using CandKey = typename std::conditional<DType<DT>::kKeyBits == 16, uint16_t, u
 template <int N>
 using Loads = std::integral_constant<int, N>;
 // How a pass reads the row: through the non-coherent path, through L2 only,
-// or (the final read) with an L2 evict-first hint.
-enum ReadKind { kReadNc, kReadCg, kReadLast };
+// through the non-coherent path with an L2 evict-first hint (the one read of
+// a row that is never read again), or (the final read of a row read more
+// than once) with an L2 evict-first hint.
+enum ReadKind { kReadNc, kReadCg, kReadNcFirst, kReadLast };
 template <int R>
 using ReadAs = std::integral_constant<int, R>;
 
@@ -420,9 +425,20 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
                : "l"(p));
   return v;
 }
+__device__ __forceinline__ uint4 ld_nc_v4_hint(const uint4* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
 
+// One row (cl.cs == 1) or one slice of a row split over a cluster.  Every
+// branch that leads to a cluster collective depends only on the row's
+// parameters or on results of earlier collectives, so all CTAs of a cluster
+// run the same collectives in the same order.
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
+__device__ __forceinline__ void apply_row(const ApplyArgs& a, const Clu& cl, unsigned char* smem) {
   using D = DType<DT>;
   using P = Packed<DT>;
   using raw = typename D::raw;
@@ -435,7 +451,6 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   // list entries per warp: the raw value and its position in the row
   constexpr int CAPW = (int)(kApplyBigBytes / (sizeof(ckey) + 4)) / kWarps / 2 * 2;
 
-  extern __shared__ __align__(128) unsigned char smem[];
   ApplyHdr& h = *reinterpret_cast<ApplyHdr*>(smem);
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kApplyHdrBytes);
   unsigned char* aux = smem + kApplyHdrBytes + kApplyHistBytes;
@@ -448,7 +463,8 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const int64_t row = blockIdx.x;
+  const int64_t row = blockIdx.x / (uint32_t)cl.cs;
+  int cph = 0;  // cluster exchange phase (cluster.cuh)
   const int V = a.V;
   const raw* xr = reinterpret_cast<const raw*>(a.x) + row * a.ldx;
   raw* orow = reinterpret_cast<raw*>(a.out) + row * a.ldo;
@@ -476,9 +492,18 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   const int nvec = (V - head) / VEC;
   const int tail = V - head - nvec * VEC;
   const uint4* xv = reinterpret_cast<const uint4*>(xr + head);
-  const int per_warp = (nvec + kWarps - 1) / kWarps;
-  const int wb = min(nvec, warp * per_warp);
-  const int we = min(nvec, wb + per_warp);
+  // this CTA's slice: vectors [cv0, cv1), plus the head (first CTA) and the
+  // tail (last CTA); elements [e0, e1) of the row
+  const int cv0 = (int)((long long)nvec * cl.rank / cl.cs);
+  const int cv1 = (int)((long long)nvec * (cl.rank + 1) / cl.cs);
+  const int cn = cv1 - cv0;
+  const bool own_head = cl.rank == 0 && head > 0;
+  const bool own_tail = cl.rank == (uint32_t)cl.cs - 1u && tail > 0;
+  const int e0 = cl.rank == 0 ? 0 : head + cv0 * VEC;
+  const int e1 = cl.rank == (uint32_t)cl.cs - 1u ? V : head + cv1 * VEC;
+  const int per_warp = (cn + kWarps - 1) / kWarps;
+  const int wb = cv0 + min(cn, warp * per_warp);
+  const int we = cv0 + min(cn, warp * per_warp + per_warp);
   const int nsteps = (we - wb + 31) / 32;  // warp-uniform
   const bool vec_out = ((reinterpret_cast<uintptr_t>(orow) ^ xaddr) & 15u) == 0;
   const uint32_t NEG2 = P::splat((uint32_t)D::kNegInf);
@@ -505,16 +530,17 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   auto load_vec = [&](auto L_c, const uint4* a) -> uint4 {
     constexpr int L = decltype(L_c)::value;
     if constexpr (L == kReadLast) return ld_global_hint(a, pol_first);
+    else if constexpr (L == kReadNcFirst) return ld_nc_v4_hint(a, pol_first);
     else if constexpr (L == kReadNc) return ld_nc_v4(a);
     else return __ldcg(a);
   };
   // n elements from row offset e0 as a vector, the rest -inf
-  auto load_partial = [&](int e0, int n) -> uint4 {
+  auto load_partial = [&](int ep, int n) -> uint4 {
     uint32_t w[4] = {NEG2, NEG2, NEG2, NEG2};
 #pragma unroll
     for (int j = 0; j < VEC; ++j) {
       if (j < n) {
-        const uint32_t b = (uint32_t)xr[e0 + j];
+        const uint32_t b = (uint32_t)xr[ep + j];
         if (KB == 16) {
           const int sh = (j & 1) * 16;
           w[j >> 1] = (w[j >> 1] & ~(0xffffu << sh)) | (b << sh);
@@ -532,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   // vectors per lane are in flight, read as L_c (a ReadKind) says.
   auto sweep = [&](auto U_c, auto L_c, auto&& f) {
     constexpr int U = decltype(U_c)::value;
-    if (warp == 0 && head > 0) {
+    if (warp == 0 && own_head) {
       const uint4 q = load_partial(0, lane == 0 ? head : 0);
       f(0, q, lane == 0 ? head : 0);
     }
@@ -552,10 +578,10 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         }
       }
     }
-    if (warp == kWarps - 1 && tail > 0) {
-      const int e0 = head + nvec * VEC;
-      const uint4 q = load_partial(e0, lane == 0 ? tail : 0);
-      f(e0, q, lane == 0 ? tail : 0);
+    if (warp == kWarps - 1 && own_tail) {
+      const int et = head + nvec * VEC;
+      const uint4 q = load_partial(et, lane == 0 ? tail : 0);
+      f(et, q, lane == 0 ? tail : 0);
     }
   };
   // sweep() whose first load group (and the head / tail vectors) is read
@@ -571,10 +597,10 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       q[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
       if (v < we) q[u] = load_vec(L_c, xv + v);
     }
-    const uint4 hq = load_partial(0, (warp == 0 && lane == 0) ? head : 0);
-    const uint4 tq = load_partial(head + nvec * VEC, (warp == kWarps - 1 && lane == 0) ? tail : 0);
+    const uint4 hq = load_partial(0, (warp == 0 && lane == 0 && own_head) ? head : 0);
+    const uint4 tq = load_partial(head + nvec * VEC, (warp == kWarps - 1 && lane == 0 && own_tail) ? tail : 0);
     pre(q, hq, tq);
-    if (warp == 0 && head > 0) f(0, hq, lane == 0 ? head : 0);
+    if (warp == 0 && own_head) f(0, hq, lane == 0 ? head : 0);
     // the next group's loads are in flight while this group is processed
     for (int s0 = 0; s0 < nsteps; s0 += U) {
       uint4 qn[U];
@@ -594,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
 #pragma unroll
       for (int u = 0; u < U; ++u) q[u] = qn[u];
     }
-    if (warp == kWarps - 1 && tail > 0) f(head + nvec * VEC, tq, lane == 0 ? tail : 0);
+    if (warp == kWarps - 1 && own_tail) f(head + nvec * VEC, tq, lane == 0 ? tail : 0);
   };
   auto each_elem = [&](auto&& g) {
     sweep(Loads<kLoadsHeavy>{}, ReadAs<kReadNc>{}, [&](int, const uint4& q, int nv) {
@@ -640,7 +666,8 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   // k), which pass A lists, so the row is read once.  With rk = k (the sample is most of the row) L is a bound
   // by construction; otherwise it is checked after the pass: fewer than k
   // listed elements, or lists that overflow, restart the two-pass flow.
-  const int fv = min(nvec, kWarps * 32 * kLoadsHeavy);
+  // (the same in every CTA of a cluster: the smallest slice's first group)
+  const int fv = min(nvec / cl.cs, kWarps * 32 * kLoadsHeavy);
   const long long rk_want = (2LL * kv * fv * VEC + V - 1) / V;
   const int rk = (int)min((long long)kv, max(8LL, rk_want));
   const bool single = topk && !generic_only && rk <= fv && 8LL * kv <= (long long)kWarps * CAPW;
@@ -651,15 +678,16 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   // (window path) ----
   uint32_t kmax = 0;
   if (single) {
+    // the row's only read (unless the bound fails): evict-first in L2
     uint32_t L2 = 0;
     sweep_pre(
-        Loads<kLoadsHeavy>{}, ReadAs<kReadNc>{},
+        Loads<kLoadsHeavy>{}, ReadAs<kReadNcFirst>{},
         [&](const uint4 (&q)[kLoadsHeavy], const uint4& hq, const uint4& tq) {
 #pragma unroll
           for (int u = 0; u < kLoadsHeavy; ++u)
             if (wb + u * 32 + lane < we) atomicAdd(&hist[swz<kBPT>(vmax_key(q[u]) >> SHB)], 1u);
-          if (warp == 0 && lane == 0 && head > 0) atomicAdd(&hist[swz<kBPT>(vmax_key(hq) >> SHB)], 1u);
-          if (warp == kWarps - 1 && lane == 0 && tail > 0) atomicAdd(&hist[swz<kBPT>(vmax_key(tq) >> SHB)], 1u);
+          if (warp == 0 && lane == 0 && own_head) atomicAdd(&hist[swz<kBPT>(vmax_key(hq) >> SHB)], 1u);
+          if (warp == kWarps - 1 && lane == 0 && own_tail) atomicAdd(&hist[swz<kBPT>(vmax_key(tq) >> SHB)], 1u);
           __syncthreads();
           const int lb = select_desc_f<kBins / kThreads>(
               [&](int j) -> unsigned long long { return hist[swz<kBPT>(kBPT * tid + j)]; },
@@ -704,7 +732,8 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
             km = __reduce_max_sync(0xffffffffu, km);
             if (lane == 0) atomicMax(&h.maxkey, km);
             __syncthreads();
-            const uint32_t k0 = h.maxkey;
+            // one table layout for the whole cluster: the largest first-group max
+            const uint32_t k0 = (uint32_t)cl_reduce1<kClMax>(cl, h.cx, cph, h.maxkey);
             const float m0 = value_of_key<DT>(k0);
             constexpr uint32_t H = 1u << (KB - 1);
             const uint32_t kfin = order_key<DT>(D::kNegInf) + 1u;
@@ -774,6 +803,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   kmax = __reduce_max_sync(0xffffffffu, kmax);
   if (lane == 0) atomicMax(&h.maxkey, kmax);
   __syncthreads();
+  const uint32_t gmax = (uint32_t)cl_reduce1<kClMax>(cl, h.cx, cph, h.maxkey);  // the row's max key
 
   // Rows whose survivors number at most k <= V/8 end in the -inf fill and
   // scatter write (unless the cut's ties overflow the ranking).  Their fill
@@ -789,14 +819,17 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
     for (int i = tid; i < kFillBlock / 16; i += kThreads) negs[i] = make_uint4(NEG2, NEG2, NEG2, NEG2);
     fence_proxy_async_shared();
     __syncthreads();
-    const uintptr_t oaddr = reinterpret_cast<uintptr_t>(orow);
-    const int ohead = min(V, (int)(((16u - (uint32_t)(oaddr & 15u)) & 15u) / (uint32_t)sizeof(raw)));
-    const int onv = (V - ohead) / VEC;
-    for (int i = tid; i < ohead; i += kThreads) orow[i] = D::kNegInf;
-    for (int i = ohead + onv * VEC + tid; i < V; i += kThreads) orow[i] = D::kNegInf;
+    // this CTA's elements [e0, e1) of the output row
+    raw* ob = orow + e0;
+    const int n = e1 - e0;
+    const uintptr_t oaddr = reinterpret_cast<uintptr_t>(ob);
+    const int ohead = min(n, (int)(((16u - (uint32_t)(oaddr & 15u)) & 15u) / (uint32_t)sizeof(raw)));
+    const int onv = (n - ohead) / VEC;
+    for (int i = tid; i < ohead; i += kThreads) ob[i] = D::kNegInf;
+    for (int i = ohead + onv * VEC + tid; i < n; i += kThreads) ob[i] = D::kNegInf;
     if (lane == 0) {
       // lane 0 of every warp issues every kWarps-th block
-      unsigned char* dst = reinterpret_cast<unsigned char*>(orow + ohead);
+      unsigned char* dst = reinterpret_cast<unsigned char*>(ob + ohead);
       const long long body = (long long)onv * 16;
       for (long long off = (long long)warp * kFillBlock; off < body; off += (long long)kWarps * kFillBlock)
         bulk_store_s2g(dst + off, negs, (uint32_t)min(body - off, (long long)kFillBlock));
@@ -810,172 +843,205 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   bool done = keepall;          // cut found
   bool have_wtie = false;       // h.wtie holds the ties of T per warp
   bool r0_known = true;         // cut_last: r0 already counted
-  const uint32_t gmax = h.maxkey;
+  unsigned long long tie_off = 0;  // ties of T in the CTAs before this one (their slices come first)
   const MassRef mr(value_of_key<DT>(gmax));
 
   // ---------------------------------------------------- candidate path
+  // Attempt 0 (single pass): every CTA listed its slice's elements >= its
+  // own sampled bound L_r.  The union of the lists holds every element of
+  // the row >= max_r L_r, so the k-th largest of the union is the row's as
+  // soon as it is >= max_r L_r (always, with one CTA).  Otherwise, and for
+  // rows without a sampled bound, attempt 1 takes one bound for the whole
+  // cluster from the merged histogram of vector maxima and lists again.
   if (topk && !generic_only) {
-    bool listed = false;
-    if (single) {
-      if (lane == 0 && h.nseg[warp] > (uint32_t)CAPW) {
-        h.nseg[warp] = CAPW;
-        h.over = 1;
-      }
-      __syncthreads();
-      unsigned long long nl = 0;  // listed elements
-      for (int w = 0; w < kWarps; ++w) nl += h.nseg[w];
-      listed = !h.over && nl >= (unsigned long long)kv;
-      if (!listed) {
-        // the bound from the first load groups was too loose (or, fewer
-        // than k listed, above the k-th largest): start over from the
-        // whole row's vector maxima
-        __syncthreads();
-        for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
-        if (tid < kWarps) h.nseg[tid] = 0;
-        if (tid == 0) h.over = 0;
-        __syncthreads();
-        sweep(Loads<kLoadsSimple>{}, ReadAs<kReadNc>{}, [&](int, const uint4& q, int nv) {
-          if (nv) atomicAdd(&hist[swz<kBPT>(vmax_key(q) >> SHB)], 1u);
-        });
-        __syncthreads();
-      }
-    }
-    if (!listed) {
-      const int lb = select_desc_f<kBins / kThreads>(
-          [&](int j) -> unsigned long long { return hist[swz<kBPT>(kBPT * tid + j)]; }, (unsigned long long)kv, h).bin;
-      if (lb > 0) {
-        // pass B (from L2): every element >= L joins its warp's list
-        Lkey = (uint32_t)lb << SHB;
-        const uint32_t L2 = P::splat((uint32_t)raw_of_key<DT>(Lkey));
-        sweep(Loads<kLoadsSimple>{}, ReadAs<kReadNc>{}, [&](int e, const uint4& q, int nv) { append_ge(e, q, nv, L2); });
-        __syncwarp();
+    for (int attempt = single ? 0 : 1; attempt < 2 && !done; ++attempt) {
+      bool listed = false;
+      uint32_t Lmin = Lkey, Lmax = Lkey;  // smallest / largest bound of the cluster
+      if (attempt == 0) {
         if (lane == 0 && h.nseg[warp] > (uint32_t)CAPW) {
           h.nseg[warp] = CAPW;
           h.over = 1;
         }
         __syncthreads();
-        listed = !h.over;
-      }
-    }
-    {
-      if (listed) {
-        // ---- select on the lists (every element >= the k-th largest is listed) ----
-        const int myn = (int)h.nseg[warp];
-        auto each_own = [&](auto&& f) {
-          for (int j = lane; j < myn; j += 32) f(order_key<DT>((raw)seg[j]));
-        };
-        if (KB == 16 && gmax - Lkey < (uint32_t)kBins) {
-          // exact per-key counts over [L, max]: a 16-bit key is a value
+        unsigned long long nl = 0;  // listed elements
+        for (int w = 0; w < kWarps; ++w) nl += h.nseg[w];
+        unsigned long long s2[2] = {(unsigned long long)h.over, nl};
+        cl_reduce<kClSum, 2>(cl, h.cx, cph, s2);
+        unsigned long long m2[2] = {(unsigned long long)Lkey, (unsigned long long)(0xffffffffu - Lkey)};
+        cl_reduce<kClMax, 2>(cl, h.cx, cph, m2);
+        Lmax = (uint32_t)m2[0];
+        Lmin = 0xffffffffu - (uint32_t)m2[1];
+        listed = s2[0] == 0 && s2[1] >= (unsigned long long)kv;
+      } else {
+        if (single) {
+          // the sampled bounds were too loose (or too high): start over from
+          // the slices' vector maxima
+          __syncthreads();
           for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+          if (tid < kWarps) h.nseg[tid] = 0;
+          if (tid == 0) h.over = 0;
           __syncthreads();
-          each_own([&](uint32_t key) { atomicAdd(&hist[swz<kBPT>(key - Lkey)], 1u); });
+          sweep(Loads<kLoadsSimple>{}, ReadAs<kReadNc>{}, [&](int, const uint4& q, int nv) {
+            if (nv) atomicAdd(&hist[swz<kBPT>(vmax_key(q) >> SHB)], 1u);
+          });
           __syncthreads();
-          auto cnt = [&](int j) -> unsigned long long { return hist[swz<kBPT>(kBPT * tid + j)]; };
-          const int bk = select_desc_f<kBPT>(cnt, (unsigned long long)kv, h).bin;
-          T = Lkey + (uint32_t)bk;
-          if (topp) {
-            bool last;
-            const Sel sp = mass_cut<DT>(
-                (int)(gmax - Lkey) + 1, bk, [&](int i) { return hist[swz<kBPT>(i)]; },
-                [&](int i) { return Lkey + (uint32_t)i; }, [](int) { return true; }, mr, thr, h, &last);
-            if (last) {
-              cut_last = true;
-              r0 = hist[swz<kBPT>(gmax - Lkey)] - 1ull;
-            } else {
-              T = (uint32_t)sp.bin;
-              r0 = sp.off;
-            }
+        }
+        cl_merge<uint32_t, kBins / 4 / kThreads>(cl, hist, kBins);
+        const int lb = select_desc_f<kBins / kThreads>(
+            [&](int j) -> unsigned long long { return hist[swz<kBPT>(kBPT * tid + j)]; }, (unsigned long long)kv, h).bin;
+        if (lb > 0) {
+          // pass B (from L2): every element >= L joins its warp's list
+          Lkey = Lmin = Lmax = (uint32_t)lb << SHB;
+          const uint32_t L2 = P::splat((uint32_t)raw_of_key<DT>(Lkey));
+          sweep(Loads<kLoadsSimple>{}, ReadAs<kReadNc>{}, [&](int e, const uint4& q, int nv) { append_ge(e, q, nv, L2); });
+          __syncwarp();
+          if (lane == 0 && h.nseg[warp] > (uint32_t)CAPW) {
+            h.nseg[warp] = CAPW;
+            h.over = 1;
           }
-        } else {
-          // 8-bit radix digits over the list keys
-          constexpr int NL = KB / 8;
-          uint32_t prefix = 0;
-          unsigned long long rank = (unsigned long long)kv;
-          for (int l = 0; l < NL; ++l) {
-            const int sh = KB - 8 * (l + 1);
-            for (int i = tid; i < kSmallBins; i += kThreads) h.small_cnt[i] = 0;
-            __syncthreads();
-            each_own([&](uint32_t key) {
-              if (l == 0 || (key >> (sh + 8)) == prefix) atomicAdd(&h.small_cnt[(key >> sh) & 255u], 1u);
-            });
-            __syncthreads();
-            unsigned long long cb[1];
-            load_bins(h.small_cnt, kSmallBins, cb);
-            const Sel sd = select_desc(cb, rank, h);
-            prefix = (prefix << 8) | (uint32_t)max(sd.bin, 0);
-            rank -= sd.off;
-          }
-          const uint32_t kkey = prefix;
-          T = kkey;
-          if (topp) {
-            unsigned long long mine = 0;
-            each_own([&](uint32_t key) {
-              if (key >= kkey) mine += mass_fixed(value_of_key<DT>(key), mr);
-            });
-            const unsigned long long S = block_sum(mine, h.ws);
-            unsigned long long rem = mass_target(thr, S);
-            uint32_t pp = 0;
-            for (int l = 0; l < NL && !cut_last; ++l) {
-              const int sh = KB - 8 * (l + 1);
-              for (int i = tid; i < kSmallBins; i += kThreads) h.small_mass[i] = 0;
-              __syncthreads();
-              each_own([&](uint32_t key) {
-                if (key >= kkey && (l == 0 || (key >> (sh + 8)) == pp)) {
-                  const unsigned long long w = mass_fixed(value_of_key<DT>(key), mr);
-                  if (w) atomicAdd(&h.small_mass[(key >> sh) & 255u], w);
-                }
-              });
-              __syncthreads();
-              unsigned long long mb[1];
-              load_bins(h.small_mass, kSmallBins, mb);
-              const Sel sa = select_asc(mb, rem, h);
-              if (sa.bin < 0) {
-                cut_last = true;  // only possible at the first level
-              } else {
-                pp = (pp << 8) | (uint32_t)sa.bin;
-                rem -= sa.off;
-              }
-            }
-            if (cut_last) {
-              uint32_t cm = 0;
-              each_own([&](uint32_t key) { cm += (key == gmax); });
-              r0 = block_sum(cm, h.ws) - 1ull;
-            } else {
-              T = pp;
-              const unsigned long long u = mass_fixed(value_of_key<DT>(T), mr);
-              r0 = u ? rem / u : 0ull;
-            }
+          __syncthreads();
+          listed = cl_reduce1<kClSum>(cl, h.cx, cph, (unsigned long long)h.over) == 0;
+        }
+      }
+      if (!listed) continue;
+      // ---- select on the lists (every element >= the k-th largest is listed) ----
+      T = 0;
+      r0 = 0;
+      cut_last = false;
+      const int myn = (int)h.nseg[warp];
+      auto each_own = [&](auto&& f) {
+        for (int j = lane; j < myn; j += 32) f(order_key<DT>((raw)seg[j]));
+      };
+      if (KB == 16 && gmax - Lmin < (uint32_t)kBins) {
+        // exact per-key counts over [Lmin, max]: a 16-bit key is a value
+        for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+        __syncthreads();
+        each_own([&](uint32_t key) { atomicAdd(&hist[swz<kBPT>(key - Lmin)], 1u); });
+        __syncthreads();
+        cl_merge<uint32_t, kBins / 4 / kThreads>(cl, hist, kBins);
+        auto cnt = [&](int j) -> unsigned long long { return hist[swz<kBPT>(kBPT * tid + j)]; };
+        const int bk = select_desc_f<kBPT>(cnt, (unsigned long long)kv, h).bin;
+        T = Lmin + (uint32_t)bk;
+        if (T < Lmax) continue;  // the lists may miss elements above the k-th largest
+        if (topp) {
+          bool last;
+          const Sel sp = mass_cut<DT>(
+              (int)(gmax - Lmin) + 1, bk, [&](int i) { return hist[swz<kBPT>(i)]; },
+              [&](int i) { return Lmin + (uint32_t)i; }, [](int) { return true; }, mr, thr, h, &last);
+          if (last) {
+            cut_last = true;
+            r0 = hist[swz<kBPT>(gmax - Lmin)] - 1ull;
+          } else {
+            T = (uint32_t)sp.bin;
+            r0 = sp.off;
           }
         }
-        if (cut_last) T = gmax;
-        done = true;
-        // ties of T per warp, from the lists (T >= L is listed)
-        uint32_t ct = 0, cgt = 0;
-        each_own([&](uint32_t key) {
-          ct += (key == T);
-          cgt += (key > T);
-        });
-        ct = __reduce_add_sync(0xffffffffu, ct);
-        if (lane == 0) h.wtie[warp] = ct;
-        have_wtie = true;
-        // The survivors are listed with their positions: when they are few,
-        // the write fills the row with -inf and scatters them, without a
-        // second read of the row.  Ties of T are ranked by position.
-        const unsigned long long ngt = block_sum(cgt, h.ws);
-        unsigned long long nties = 0;
-        for (int w = 0; w < kWarps; ++w) nties += h.wtie[w];
+      } else {
+        // 8-bit radix digits over the list keys
+        constexpr int NL = KB / 8;
+        uint32_t prefix = 0;
+        unsigned long long rank = (unsigned long long)kv;
+        for (int l = 0; l < NL; ++l) {
+          const int sh = KB - 8 * (l + 1);
+          for (int i = tid; i < kSmallBins; i += kThreads) h.small_cnt[i] = 0;
+          __syncthreads();
+          each_own([&](uint32_t key) {
+            if (l == 0 || (key >> (sh + 8)) == prefix) atomicAdd(&h.small_cnt[(key >> sh) & 255u], 1u);
+          });
+          __syncthreads();
+          cl_merge<uint32_t, 1>(cl, h.small_cnt, kSmallBins);
+          unsigned long long cb[1];
+          load_bins(h.small_cnt, kSmallBins, cb);
+          const Sel sd = select_desc(cb, rank, h);
+          prefix = (prefix << 8) | (uint32_t)max(sd.bin, 0);
+          rank -= sd.off;
+        }
+        const uint32_t kkey = prefix;
+        T = kkey;
+        if (T < Lmax) continue;  // the lists may miss elements above the k-th largest
+        if (topp) {
+          unsigned long long mine = 0;
+          each_own([&](uint32_t key) {
+            if (key >= kkey) mine += mass_fixed(value_of_key<DT>(key), mr);
+          });
+          const unsigned long long S = cl_reduce1<kClSum>(cl, h.cx, cph, block_sum(mine, h.ws));
+          unsigned long long rem = mass_target(thr, S);
+          uint32_t pp = 0;
+          for (int l = 0; l < NL && !cut_last; ++l) {
+            const int sh = KB - 8 * (l + 1);
+            for (int i = tid; i < kSmallBins; i += kThreads) h.small_mass[i] = 0;
+            __syncthreads();
+            each_own([&](uint32_t key) {
+              if (key >= kkey && (l == 0 || (key >> (sh + 8)) == pp)) {
+                const unsigned long long w = mass_fixed(value_of_key<DT>(key), mr);
+                if (w) atomicAdd(&h.small_mass[(key >> sh) & 255u], w);
+              }
+            });
+            __syncthreads();
+            cl_merge<unsigned long long, 1>(cl, h.small_mass, kSmallBins);
+            unsigned long long mb[1];
+            load_bins(h.small_mass, kSmallBins, mb);
+            const Sel sa = select_asc(mb, rem, h);
+            if (sa.bin < 0) {
+              cut_last = true;  // only possible at the first level
+            } else {
+              pp = (pp << 8) | (uint32_t)sa.bin;
+              rem -= sa.off;
+            }
+          }
+          if (cut_last) {
+            uint32_t cm = 0;
+            each_own([&](uint32_t key) { cm += (key == gmax); });
+            r0 = cl_reduce1<kClSum>(cl, h.cx, cph, block_sum(cm, h.ws)) - 1ull;
+          } else {
+            T = pp;
+            const unsigned long long u = mass_fixed(value_of_key<DT>(T), mr);
+            r0 = u ? rem / u : 0ull;
+          }
+        }
+      }
+      if (cut_last) T = gmax;
+      done = true;
+      // ties of T per warp, from the lists (T >= L is listed)
+      uint32_t ct = 0, cgt = 0;
+      each_own([&](uint32_t key) {
+        ct += (key == T);
+        cgt += (key > T);
+      });
+      ct = __reduce_add_sync(0xffffffffu, ct);
+      if (lane == 0) h.wtie[warp] = ct;
+      have_wtie = true;
+      // The survivors are listed with their positions: when they are few,
+      // the write fills the row with -inf and scatters them, without a
+      // second read of the row.  Ties of T are ranked by position: this
+      // CTA's ties follow the tie_off ties of the CTAs before it.
+      const unsigned long long ngt_mine = block_sum(cgt, h.ws);
+      unsigned long long nt_mine = 0;
+      for (int w = 0; w < kWarps; ++w) nt_mine += h.wtie[w];
+      {
+        const unsigned long long v2[2] = {nt_mine, ngt_mine};
+        unsigned long long ex2[2], tot2[2];
+        cl_prefix<2>(cl, h.cx, cph, v2, ex2, tot2);
+        tie_off = ex2[0];
+        const unsigned long long nties = tot2[0], ngt = tot2[1];
         const bool fill = ngt + (nties - r0) <= (unsigned long long)(V / 8) && (r0 == 0 || nties <= kTieRankMax);
         if (fill && r0 > 0) {
+          // this CTA masks its first rl ties (all of them: tie_cut past every position)
+          const unsigned long long rl = r0 > tie_off ? min(r0 - tie_off, nt_mine) : 0ull;
           uint32_t* tpos = hist;  // free again: positions of the ties of T
           for (int j = lane; j < myn; j += 32)
             if (order_key<DT>((raw)seg[j]) == T) tpos[atomicAdd(&h.ntie, 1u)] = segi[j];
           __syncthreads();
           const int nt = (int)h.ntie;
-          for (int t = tid; t < nt; t += kThreads) {
-            const uint32_t mine = tpos[t];
-            int rank = 0;
-            for (int u = 0; u < nt; ++u) rank += tpos[u] < mine;
-            if (rank == (int)r0) h.tie_cut = mine;  // the first tie that stays
+          if (rl == (unsigned long long)nt) {
+            if (tid == 0) h.tie_cut = 0xffffffffu;
+          } else {
+            for (int t2 = tid; t2 < nt; t2 += kThreads) {
+              const uint32_t mine = tpos[t2];
+              int rank = 0;
+              for (int u = 0; u < nt; ++u) rank += tpos[u] < mine;
+              if (rank == (int)rl) h.tie_cut = mine;  // the first tie that stays
+            }
           }
         }
         if (tid == 0) h.fill = fill ? 1u : 0u;
@@ -994,6 +1060,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   bool window_counted = !masstab;  // the window path's bucket counts exist
   if (masstab) {
     uint32_t* tab = kcount;
+    cl_sync(cl);  // every CTA's table is complete: read the cluster's sums through cl_sum_at
     const uint32_t ta = h.mt_a, tb = h.mt_b, tfloor = h.mt_floor, k0 = h.mt_k0, lump = h.mt_lump;
     const int qn = h.mt_qn;
     constexpr uint32_t H = 1u << (KB - 1);
@@ -1013,7 +1080,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       const bool shared_floor = lump && tfloor > 0;
       bool last;
       const Sel sp = mass_cut<DT>(
-          (int)gbin + 1, 0, [&](int v) { return tab[v]; }, key_of,
+          (int)gbin + 1, 0, [&](int v) { return cl_sum_at(cl, tab, v); }, key_of,
           [&](int v) { return !(shared_floor && v == qn); }, mr, thr, h, &last);
       if (last) {
         cut_last = true;
@@ -1026,6 +1093,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         done = true;
       }
     }
+    cl_sync(cl);  // no peer reads this CTA's table any more
     if (!done) {
       // fall back to the window path: it needs the bucket counts
       __syncthreads();
@@ -1047,6 +1115,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   // ------------------------------------------------------- window path
   if (window && !done && window_counted) {
     constexpr int BPT = kBins / kThreads;  // thread t owns buckets BPT*t .. BPT*t+BPT-1
+    cl_merge<uint32_t, kBins / 4 / kThreads>(cl, hist, kBins);
     unsigned long long* lo_m = reinterpret_cast<unsigned long long*>(big);  // [kBins]
     unsigned long long* hi_m = lo_m + kBins;                                // [kBins]
     // rigorous bounds of each bucket's mass: counts times the mass of the
@@ -1183,8 +1252,10 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       });
       s_mine += f2ull_rn(s_run * kMassScaleF);
       b_mine += f2ull_rn(b_run * kMassScaleF);
-      unsigned long long d0, d1, S, below;
-      block_exclusive_scan2(s_mine, b_mine, &d0, &d1, &S, &below, h.ws);
+      unsigned long long d0, d1, sb[2];
+      block_exclusive_scan2(s_mine, b_mine, &d0, &d1, &sb[0], &sb[1], h.ws);
+      cl_reduce<kClSum, 2>(cl, h.cx, cph, sb);  // (its barrier also completes every CTA's window counters)
+      const unsigned long long S = sb[0], below = sb[1];
       const unsigned long long target = mass_target(thr, S);
       if (target >= S) {
         // only the last sorted position survives: the last element equal to the max
@@ -1200,7 +1271,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
           unsigned long long m = 0;
           if (blk < nblk) {
             const uint32_t key = ((uint32_t)bucket_of[blk] << SHB) | (uint32_t)(lane & 15);
-            const uint32_t c = kcount[blk * 16 + (lane & 15)];
+            const uint32_t c = cl_sum_at(cl, kcount, (int)(blk * 16 + (lane & 15)));
             if (c) m = (unsigned long long)c * mass_fixed(value_of_key<DT>(key), mr);
           }
 #pragma unroll
@@ -1222,9 +1293,9 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
           for (int j = 0; j < BPT; ++j) {
             if (tw < acc + mb[j]) {
               const uint32_t b = (uint32_t)(BPT * tid + j);
-              const uint32_t* cb = kcount + block_of[b] * 16;
+              const int cb = (int)(block_of[b] * 16);
               for (int kk = 0; kk < 16; ++kk) {
-                const uint32_t c = cb[kk];
+                const uint32_t c = cl_sum_at(cl, kcount, cb + kk);
                 if (!c) continue;
                 const uint32_t key = (b << SHB) | (uint32_t)kk;
                 const unsigned long long u = mass_fixed(value_of_key<DT>(key), mr);
@@ -1248,6 +1319,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
           done = true;
         }
       }
+      cl_sync(cl);  // no peer reads this CTA's window counters any more
     }
   }
 
@@ -1275,6 +1347,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       __syncthreads();
       each_elem([&](raw r) { atomicAdd(&hist[order_key<DT>(r) >> SH1], 1u); });
       __syncthreads();
+      cl_merge<uint32_t, 2048 / 4 / kThreads>(cl, hist, 2048);
       unsigned long long cb[2048 / kThreads];
       load_bins(hist, 2048, cb);
       const Sel g0 = select_desc(cb, (unsigned long long)kv, h);
@@ -1289,6 +1362,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
           if ((key >> shp) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
         });
         __syncthreads();
+        cl_merge<uint32_t, 2048 / 4 / kThreads>(cl, hist, nb);
         unsigned long long lb2[2048 / kThreads];
         load_bins(hist, nb, lb2);
         const Sel gl = select_desc(lb2, rank, h);
@@ -1310,6 +1384,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
         }
       });
       __syncthreads();
+      cl_merge<unsigned long long, 2048 * 2 / 4 / kThreads>(cl, mass, 2048);
       unsigned long long mb[2048 / kThreads];
       load_bins(mass, 2048, mb);
       unsigned long long part = 0;
@@ -1335,6 +1410,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
             }
           });
           __syncthreads();
+          cl_merge<unsigned long long, 2048 * 2 / 4 / kThreads>(cl, mass, nb);
           unsigned long long lb2[2048 / kThreads];
           load_bins(mass, nb, lb2);
           const Sel gq = select_asc(lb2, rem, h);
@@ -1367,13 +1443,16 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   // ---- write: the listed survivors over a -inf row ([guide] §2 step 8) ----
   if (h.fill) {
     if (!early_fill) {
-      const uintptr_t oaddr = reinterpret_cast<uintptr_t>(orow);
-      const int ohead = min(V, (int)(((16u - (uint32_t)(oaddr & 15u)) & 15u) / (uint32_t)sizeof(raw)));
-      const int onv = (V - ohead) / VEC;
-      for (int i = tid; i < ohead; i += kThreads) orow[i] = D::kNegInf;
-      uint4* ov = reinterpret_cast<uint4*>(orow + ohead);
+      // this CTA's elements [e0, e1) of the output row
+      raw* ob = orow + e0;
+      const int n = e1 - e0;
+      const uintptr_t oaddr = reinterpret_cast<uintptr_t>(ob);
+      const int ohead = min(n, (int)(((16u - (uint32_t)(oaddr & 15u)) & 15u) / (uint32_t)sizeof(raw)));
+      const int onv = (n - ohead) / VEC;
+      for (int i = tid; i < ohead; i += kThreads) ob[i] = D::kNegInf;
+      uint4* ov = reinterpret_cast<uint4*>(ob + ohead);
       for (int i = tid; i < onv; i += kThreads) st_global_hint(ov + i, make_uint4(NEG2, NEG2, NEG2, NEG2), pol_first);
-      for (int i = ohead + onv * VEC + tid; i < V; i += kThreads) orow[i] = D::kNegInf;
+      for (int i = ohead + onv * VEC + tid; i < n; i += kThreads) ob[i] = D::kNegInf;
       __syncthreads();
     }
     const int myn = (int)h.nseg[warp];
@@ -1396,7 +1475,7 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
       if (r0 == 0) {
         rule = kTiesKept;
       } else {
-        unsigned long long pre = 0;
+        unsigned long long pre = tie_off;  // ties in the CTAs before this one come first
         for (int w = 0; w < warp; ++w) pre += h.wtie[w];
         const unsigned long long mine = h.wtie[warp];
         rule = (pre + mine <= r0) ? kTiesMasked : (pre >= r0 ? kTiesKept : kTiesStraddle);
@@ -1493,13 +1572,22 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   });
   if (lane == 0) h.wtie[warp] = wn;
   __syncthreads();
-  unsigned long long all = 0, pre = 0;
-  bool overflow = false;
+  unsigned long long all_mine = 0, pre = 0, overflow = 0;
   for (int w = 0; w < kWarps; ++w) {
     if (w < warp) pre += h.wtie[w];
-    all += h.wtie[w];
-    overflow |= h.wtie[w] > (uint32_t)kTieCap;
+    all_mine += h.wtie[w];
+    overflow += h.wtie[w] > (uint32_t)kTieCap ? 1u : 0u;
   }
+  unsigned long long all;
+  {
+    const unsigned long long v2[2] = {all_mine, overflow};
+    unsigned long long ex2[2], tot2[2];
+    cl_prefix<2>(cl, h.cx, cph, v2, ex2, tot2);
+    tie_off = ex2[0];
+    all = tot2[0];
+    overflow = tot2[1];
+  }
+  pre += tie_off;
   if (!r0_known) r0 = all - 1ull;  // only the last sorted position survives: the last element equal to the max
   if (overflow) {
     write_ranked();
@@ -1507,6 +1595,14 @@ __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   }
   for (uint32_t j = lane; j < wn; j += 32)
     if (pre + j < r0) orow[tpos[j]] = D::kNegInf;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Clu cl{a.cs, a.cs > 1 ? cluster_ctarank() : 0u};
+  apply_row<DT>(a, cl, smem);
+  cluster_fence_exit(cl);
 }
 
 template <int DT>
@@ -1520,8 +1616,19 @@ static cudaError_t launch_one(const ApplyArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  kern<<<dim3((unsigned)a.B), dim3(kThreads), kApplySmem, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.B * a.cs));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kApplySmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)a.cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.cs > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 cudaError_t launch_apply(topkp_dtype dt, const ApplyArgs& a, cudaStream_t s) {

@@ -9,9 +9,11 @@
 namespace topkp {
 
 // ---------------------------------------------------------------- apply
-// One CTA filters one row.  Warp w owns the w-th sixteenth of the row's
-// 16-byte vectors and reads them straight into registers: once from HBM,
-// then again from L2 for the later passes.
+// A cluster of cs CTAs filters one row (cs = 1: one CTA, no cluster); each
+// CTA owns a contiguous slice of the row's 16-byte vectors, and warp w of a
+// CTA the w-th sixteenth of its slice, read straight into registers: once
+// from HBM, then again from L2 for the later passes.  Every reduction over
+// the row goes through the cluster's distributed shared memory.
 struct ApplyArgs {
   const void* x;          // logits [B, ldx]
   void* out;              // out [B, ldo]
@@ -20,22 +22,31 @@ struct ApplyArgs {
   int64_t ldx, ldo;       // row strides, elements
   int64_t B;
   int32_t V;
+  int32_t cs;             // CTAs per row (cluster size: 1, 2, 4 or 8)
   int32_t force;          // kApplyForce* bits (testing: route rows to one path)
 };
 
 // Every row that needs a cut takes the generic radix path.
 constexpr int32_t kApplyForceGeneric = 1;
 
-// Shared memory of one apply CTA: header (small histograms, scan scratch),
-// a 4096-entry table (bucket histogram, or bucket -> count block), a 10 KB
-// auxiliary region (count block -> bucket, block masses), and a 64 KB region
-// for the per-key count blocks (or the per-warp candidate lists, or the
-// generic path's mass bins).
+// Shared memory of one apply CTA: header (small histograms, scan scratch,
+// cluster exchange slots), a 4096-entry table (bucket histogram, or bucket
+// -> count block), a 10 KB auxiliary region (count block -> bucket, block
+// masses), and a 64 KB region for the per-key count blocks (or the per-warp
+// candidate lists, or the generic path's mass bins).
 constexpr size_t kApplyHdrBytes = 4096;
 constexpr size_t kApplyHistBytes = 4096 * 4;
 constexpr size_t kApplyAuxBytes = 1024 * 2 + 1024 * 8;
 constexpr size_t kApplyBigBytes = 65536;
 constexpr size_t kApplySmem = kApplyHdrBytes + kApplyHistBytes + kApplyAuxBytes + kApplyBigBytes;
+
+// CTAs per row for a batch of B rows of length V on num_sms SMs: rows are
+// split while the split batch still runs as one resident wave (two CTAs per
+// SM) and every slice keeps at least kApplyMinSlice elements.  force
+// (testing) may name a size: "c1", "c2", "c4" or "c8", alone or after
+// "generic,".
+constexpr int64_t kApplyMinSlice = 4096;
+int plan_apply(int64_t B, int64_t V, int num_sms, const char* force, int32_t* force_bits);
 
 cudaError_t launch_apply(topkp_dtype dt, const ApplyArgs& a, cudaStream_t s);
 
