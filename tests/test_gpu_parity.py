@@ -90,9 +90,10 @@ def _check_all(out, x, dtype, p, k, where, infos=None):
 
 # TOPKP_FORCE_PLAN: "" = the planner's choice; "generic" = every row that
 # needs a cut takes the generic radix path; "cN" = every row is split over a
-# cluster of N CTAs (slices may be short or empty), alone or after
-# "generic,".
-PLANS = ["", "generic", "c2", "c8", "generic,c4"]
+# cluster of N CTAs (slices may be short or empty), "mN" = mixed clusters of
+# N (a row without top-k split over the cluster, or N rows with top-k, one
+# per CTA), alone or after "generic,".
+PLANS = ["", "generic", "c2", "c8", "generic,c4", "m4"]
 
 
 @pytest.mark.parametrize("dtype", DTS)
@@ -225,7 +226,7 @@ def test_workload3_every_split_full_size(tk, monkeypatch):
     dt = w["dtype"]
     xt, pt, kt = _workload_inputs(w)
     infos = _infos(w["x"], dt, w["p"], w["k"])
-    for plan in ("c1", "c2", "c4", "c8", ""):
+    for plan in ("c1", "c2", "c4", "c8", "m2", "m8", ""):
         monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
         out = torch_to_raw(tk.apply(xt, p=pt, k=kt), dt)
         tk.device_status()

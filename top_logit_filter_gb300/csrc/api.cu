@@ -77,26 +77,42 @@ void report_launches(int n) { g_last_launches = n; }
 int device_sms(int* dev) { return current_sms(dev); }
 
 // ------------------------------------------------------------------ planners
-int plan_apply(int64_t B, int64_t V, int num_sms, const char* force, int32_t* force_bits) {
-  *force_bits = 0;
+ApplyPlan plan_apply(int64_t B, int64_t V, bool has_k, int num_sms, const char* force) {
+  ApplyPlan pl;
   int cs = 0;
   if (force && *force) {
     const char* f = force;
     if (strncmp(f, "generic", 7) == 0) {
-      *force_bits |= kApplyForceGeneric;
+      pl.force_bits |= kApplyForceGeneric;
       f += 7;
       if (*f == ',') ++f;
     }
-    if (*f == 'c') cs = atoi(f + 1);
-    if (cs != 1 && cs != 2 && cs != 4 && cs != 8) cs = 0;
+    if (*f == 'c' || *f == 'm') {
+      pl.mixed = *f == 'm';
+      cs = atoi(f + 1);
+    }
+    if (cs != 1 && cs != 2 && cs != 4 && cs != 8) {
+      cs = 0;
+      pl.mixed = 0;
+    }
   }
   if (cs == 0) {
-    // split rows while the split batch still runs as one resident wave (two
-    // CTAs per SM) and each slice keeps kApplyMinSlice elements
+    // one resident wave: two CTAs per SM
+    const int64_t slots = 2LL * num_sms;
     cs = 1;
-    while (cs < 8 && B * cs * 2 <= 2LL * num_sms && V / (2 * cs) >= kApplyMinSlice) cs *= 2;
+    if (!has_k) {
+      while (cs < 8 && B * cs * 2 <= slots && V / (2 * cs) >= kApplyMinSlice) cs *= 2;
+    } else {
+      // mixed clusters of 2c CTAs: the dense rows take 2c CTAs each, the
+      // others one, and clusters are filled
+      const int64_t dense = (B + kApplyDenseShare - 1) / kApplyDenseShare;
+      while (cs < 8 && dense * 2 * cs + (B - dense) + 2 * cs <= slots && V / (2 * cs) >= kApplyMinSlice) cs *= 2;
+      pl.mixed = cs > 1;
+    }
   }
-  return cs;
+  if (!has_k) pl.mixed = 0;  // every row is dense: plain clusters
+  pl.cs = cs;
+  return pl;
 }
 
 static int slice_for(int64_t V, int C) {
@@ -172,7 +188,10 @@ topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_lo
   a.ldx = ld_logits;
   a.ldo = ld_out;
   a.V = (int32_t)V;
-  a.cs = plan_apply(B, V, sms, getenv("TOPKP_FORCE_PLAN"), &a.force);
+  const ApplyPlan plan = plan_apply(B, V, k != nullptr, sms, getenv("TOPKP_FORCE_PLAN"));
+  a.cs = plan.cs;
+  a.mixed = plan.mixed;
+  a.force = plan.force_bits;
   // cs CTAs per row; grid.x must stay below 2^31
   const int64_t max_rows = INT_MAX / a.cs;
   int launches = 0;

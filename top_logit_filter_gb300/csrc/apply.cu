@@ -438,7 +438,7 @@ __device__ __forceinline__ uint4 ld_nc_v4_hint(const uint4* p, uint64_t pol) {
 // parameters or on results of earlier collectives, so all CTAs of a cluster
 // run the same collectives in the same order.
 template <int DT>
-__device__ __forceinline__ void apply_row(const ApplyArgs& a, const Clu& cl, unsigned char* smem) {
+__device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row, const Clu& cl, unsigned char* smem) {
   using D = DType<DT>;
   using P = Packed<DT>;
   using raw = typename D::raw;
@@ -463,7 +463,6 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const Clu& cl, uns
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const int64_t row = blockIdx.x / (uint32_t)cl.cs;
   int cph = 0;  // cluster exchange phase (cluster.cuh)
   const int V = a.V;
   const raw* xr = reinterpret_cast<const raw*>(a.x) + row * a.ldx;
@@ -1597,11 +1596,70 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const Clu& cl, uns
     if (pre + j < r0) orow[tpos[j]] = D::kNegInf;
 }
 
+// Mixed clusters: cluster c takes the c-th row without top-k while c < nd,
+// the number of such rows (all CTAs of the cluster split it); after that,
+// cluster c takes the rows with top-k numbered (c - nd) * cs + rank, one per
+// CTA.  Rows of a kind are numbered in index order.  Returns -1 for a CTA
+// whose number runs past its kind (it has no row).  The whole CTA calls
+// this; scratch holds kWarps + 1 words of shared memory.
+__device__ __forceinline__ int64_t mixed_row(const ApplyArgs& a, uint32_t rank, bool* split, uint32_t* scratch) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t c = blockIdx.x / (uint32_t)a.cs;
+  auto dense = [&](int64_t r) -> bool {
+    const int kv = a.k[r];
+    return !(kv >= 1 && kv <= a.V - 1);
+  };
+  uint32_t n = 0;
+  for (int64_t r = tid; r < a.B; r += kThreads) n += dense(r) ? 1u : 0u;
+  n = __reduce_add_sync(0xffffffffu, n);
+  if (lane == 0) scratch[warp] = n;
+  if (tid == 0) scratch[kWarps] = 0xffffffffu;
+  __syncthreads();
+  int64_t nd = 0;
+  for (int w = 0; w < kWarps; ++w) nd += scratch[w];
+  __syncthreads();
+  const bool want_dense = c < nd;
+  const int64_t want = want_dense ? c : (c - nd) * a.cs + rank;
+  *split = want_dense;
+  int64_t seen = 0;  // rows of the wanted kind before this round
+  for (int64_t base = 0; base < a.B && seen <= want; base += kThreads) {
+    const int64_t r = base + tid;
+    const bool m = r < a.B && dense(r) == want_dense;
+    const uint32_t bal = __ballot_sync(0xffffffffu, m);
+    if (lane == 0) scratch[warp] = (uint32_t)__popc(bal);
+    __syncthreads();
+    int64_t before = seen, tot = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int64_t x = scratch[w];
+      before += w < warp ? x : 0;
+      tot += x;
+    }
+    if (m && before + __popc(bal & ((1u << lane) - 1u)) == want) scratch[kWarps] = (uint32_t)r;
+    __syncthreads();
+    seen += tot;
+  }
+  const uint32_t found = scratch[kWarps];
+  __syncthreads();  // before the caller reuses the scratch
+  return found == 0xffffffffu ? -1 : (int64_t)found;
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 2) apply_kernel(const ApplyArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const Clu cl{a.cs, a.cs > 1 ? cluster_ctarank() : 0u};
-  apply_row<DT>(a, cl, smem);
+  const uint32_t rank = a.cs > 1 ? cluster_ctarank() : 0u;
+  int64_t row = blockIdx.x / (uint32_t)a.cs;
+  int cs = a.cs;
+  if (a.mixed) {
+    // a row with top-k reads itself once and runs on one CTA; a CTA without
+    // a row leaves at once (no collective involves it)
+    bool split = true;
+    row = mixed_row(a, rank, &split, reinterpret_cast<uint32_t*>(smem));
+    if (row < 0) return;
+    if (!split) cs = 1;
+  }
+  // a CTA that filters a row alone owns all of it (rank 0 of a cluster of one)
+  const Clu cl{cs, cs > 1 ? rank : 0u};
+  apply_row<DT>(a, row, cl, smem);
   cluster_fence_exit(cl);
 }
 

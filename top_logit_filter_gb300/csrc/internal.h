@@ -22,7 +22,8 @@ struct ApplyArgs {
   int64_t ldx, ldo;       // row strides, elements
   int64_t B;
   int32_t V;
-  int32_t cs;             // CTAs per row (cluster size: 1, 2, 4 or 8)
+  int32_t cs;             // CTAs per cluster (1, 2, 4 or 8)
+  int32_t mixed;          // clusters take one row without top-k, or cs rows with top-k (one per CTA)
   int32_t force;          // kApplyForce* bits (testing: route rows to one path)
 };
 
@@ -40,13 +41,25 @@ constexpr size_t kApplyAuxBytes = 1024 * 2 + 1024 * 8;
 constexpr size_t kApplyBigBytes = 65536;
 constexpr size_t kApplySmem = kApplyHdrBytes + kApplyHistBytes + kApplyAuxBytes + kApplyBigBytes;
 
-// CTAs per row for a batch of B rows of length V on num_sms SMs: rows are
-// split while the split batch still runs as one resident wave (two CTAs per
-// SM) and every slice keeps at least kApplyMinSlice elements.  force
-// (testing) may name a size: "c1", "c2", "c4" or "c8", alone or after
-// "generic,".
+// Launch plan of topkp_apply for a batch of B rows of length V on num_sms
+// SMs (two CTAs per SM).  Rows without top-k (top-p alone, or a copy) read
+// themselves twice; rows with top-k read themselves once.  Without k every
+// row is split over a cluster of cs CTAs while the split batch still runs as
+// one resident wave and every slice keeps at least kApplyMinSlice elements.
+// With k the clusters are mixed: a cluster takes one row without top-k,
+// split over its cs CTAs, or cs rows with top-k, one per CTA; the rows
+// without top-k come first.  cs is sized for up to one such row in
+// kApplyDenseShare.  force (testing) may name a plan: "cN" splits every row
+// over N CTAs, "mN" makes mixed clusters of N (N = 1, 2, 4, 8), alone or
+// after "generic,".
 constexpr int64_t kApplyMinSlice = 4096;
-int plan_apply(int64_t B, int64_t V, int num_sms, const char* force, int32_t* force_bits);
+constexpr int64_t kApplyDenseShare = 8;
+struct ApplyPlan {
+  int cs = 1;
+  int mixed = 0;
+  int force_bits = 0;
+};
+ApplyPlan plan_apply(int64_t B, int64_t V, bool has_k, int num_sms, const char* force);
 
 cudaError_t launch_apply(topkp_dtype dt, const ApplyArgs& a, cudaStream_t s);
 
