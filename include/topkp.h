@@ -185,6 +185,74 @@ topkp_status topkp_sample(const void* filtered, int64_t B, int64_t V, int64_t ld
                           void* out, int64_t ld_out, int32_t* token, void* stream);
 
 /*
+ * topkp_sample_v2 -- the TopKTopPSampleV2 semantics of the web page
+ * "aclnnTopKTopPSampleV2" (CANN API reference; Formula / TopK sampling,
+ * TopP sampling, minP sampling, Optional output, Subsequent processing, and
+ * Constraints).  Per row, on the row ordered from the largest value down
+ * (equal values in increasing original index):
+ *   1. top-k runs iff top_k != NULL and 1 <= top_k[b] <= min(V, ks_max
+ *      rounded up to a multiple of 8); it keeps exactly the first top_k[b]
+ *      positions (ties with the k-th value beyond them are removed);
+ *   2. the probabilities: with input_is_logits, the softmax over the
+ *      positions left; otherwise the input values themselves;
+ *   3. top-p runs iff top_p != NULL and top_p[b] < 1.  After a top-k stage a
+ *      position stays iff the probabilities before it sum to <= top_p[b];
+ *      when top-k was skipped, iff its own and every later probability sum
+ *      to > fp32(1 - top_p[b]).  The first position always stays;
+ *   4. min-p (min_p != NULL and min_p[b] > 0): positions whose probability
+ *      is below prob[0] * min_p[b] go; min_p[b] >= 1 keeps position 0 alone;
+ *   5. the token: without q, the original index of position 0; with q, of
+ *      the kept position with the largest prob / (q[b][j] + eps), where q is
+ *      read by sorted position j (first on ties).
+ * The kept positions form a prefix of the order.
+ *
+ *   logits       device, [B, V] of dtype, row stride ld_logits (>= V).
+ *   B, V         rows and row length; 0 <= V <= 2^20 ([V2] Constraints).
+ *                B == 0 or V == 0 returns TOPKP_SUCCESS without a launch.
+ *   top_k        device, [B] int32, or NULL (top-k skipped on every row).
+ *   top_p        device, [B] float, or NULL (top-p skipped).
+ *   min_p        device, [B] float, or NULL (min-p skipped).
+ *   q            device, [B, V] float, row stride ldq (>= V), or NULL (the
+ *                token is position 0).
+ *   eps          added to every q (>= 0; the page gives it no value).
+ *   ks_max       in [1, 1024]; the page's default is lost, so it is an
+ *                argument.
+ *   input_is_logits  nonzero: logits, softmax them, removed outputs -inf;
+ *                zero: the input already holds probabilities, removed
+ *                outputs 0 (the page's defLogit).
+ * Outputs (each may be NULL, not all; none may overlap an input, the
+ * workspace or another output):
+ *   select       device, [B, V] of dtype, row stride ld_select (>= V): the
+ *                input element where its position was kept, defLogit
+ *                elsewhere (logitsTopKPSelect).
+ *   token        device, [B] int32: the sampled original index
+ *                (logitsSelectIdx).
+ *   logits_idx   device, [B, V] int32, contiguous: the original index of
+ *                sorted position j for j < n (n = top_k[b] after a top-k
+ *                stage, V otherwise), -1 past n (logitsIdx).
+ *   sort_masked  device, [B, V] float, contiguous: the fp32 probability of
+ *                each kept sorted position; a position not kept holds 0 when
+ *                min-p ran or the input is probabilities, -inf otherwise
+ *                (logitsSortMasked).
+ *   workspace    device, at least topkp_sample_v2_workspace_size(B, V,
+ *                dtype) bytes, 256-byte aligned, owned by the caller (the
+ *                rows whose top-k is skipped are sorted into it; the page's
+ *                two-stage form).
+ * Results.  Probabilities are fp32 from fp32 exponentials; a top-p or min-p
+ * decision can differ from exact arithmetic only where the cumulative
+ * probability lies within 1e-5 of its threshold (or the probability within
+ * 1e-5, relative, of prob[0] * min_p), and the token only where another
+ * kept position's prob / (q + eps) lies within 1e-5 (relative) of the
+ * largest.  Deterministic.  Three kernel launches.
+ */
+size_t topkp_sample_v2_workspace_size(int64_t B, int64_t V, topkp_dtype dtype);
+topkp_status topkp_sample_v2(const void* logits, int64_t B, int64_t V, int64_t ld_logits, topkp_dtype dtype,
+                             const int32_t* top_k, const float* top_p, const float* min_p, const float* q,
+                             int64_t ldq, float eps, int32_t ks_max, int32_t input_is_logits, void* select,
+                             int64_t ld_select, int32_t* token, int32_t* logits_idx, float* sort_masked,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * topkp_sort -- the sort that aclnnApplyTopKTopP runs before the filter
  * (section 6.1 of the page: l0op::Sort with descending = false and stable =
  * true), producing the inputs of topkp_apply_sorted.  Per row:
@@ -252,8 +320,8 @@ const char* topkp_last_error_string(void);
 topkp_status topkp_device_status(void* stream);
 
 /* Number of kernel launches the most recent successful topkp_apply /
- * topkp_apply_sorted / topkp_sample / topkp_sort call on this thread
- * enqueued (0 for an empty problem). */
+ * topkp_apply_sorted / topkp_sample / topkp_sample_v2 / topkp_sort call on
+ * this thread enqueued (0 for an empty problem). */
 int topkp_last_launch_count(void);
 
 #ifdef __cplusplus

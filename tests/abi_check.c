@@ -60,6 +60,38 @@ int main(void) {
     printf("FAIL: launches counted for an empty problem\n");
     ++failures;
   }
+  /* topkp_sample_v2: checks before any device work */
+  {
+    int32_t* fake_idx = (int32_t*)((uintptr_t)(1u << 20) + 16384);
+    expect("sample_v2, ks_max 0",
+           topkp_sample_v2(fake, 2, 8, 8, TOPKP_BF16, fake_k, NULL, NULL, NULL, 8, 0.0f, 0, 1, NULL, 8, fake_tok,
+                           NULL, NULL, fake_out, 1u << 20, NULL),
+           TOPKP_ERR_PARAM_INVALID);
+    expect("sample_v2, ks_max 1025",
+           topkp_sample_v2(fake, 2, 8, 8, TOPKP_BF16, fake_k, NULL, NULL, NULL, 8, 0.0f, 1025, 1, NULL, 8, fake_tok,
+                           NULL, NULL, fake_out, 1u << 20, NULL),
+           TOPKP_ERR_PARAM_INVALID);
+    expect("sample_v2, no output",
+           topkp_sample_v2(fake, 2, 8, 8, TOPKP_BF16, fake_k, NULL, NULL, NULL, 8, 0.0f, 64, 1, NULL, 8, NULL, NULL,
+                           NULL, fake_out, 1u << 20, NULL),
+           TOPKP_ERR_PARAM_NULLPTR);
+    expect("sample_v2, V above 2^20",
+           topkp_sample_v2(fake, 2, (1 << 20) + 1, (1 << 20) + 1, TOPKP_F32, NULL, NULL, NULL, NULL, 8, 0.0f, 64, 1,
+                           NULL, 8, fake_tok, NULL, NULL, fake_out, 1u << 20, NULL),
+           TOPKP_ERR_PARAM_INVALID);
+    expect("sample_v2, workspace too small",
+           topkp_sample_v2(fake, 2, 8, 8, TOPKP_BF16, fake_k, NULL, NULL, NULL, 8, 0.0f, 64, 1, NULL, 8, fake_tok,
+                           fake_idx, NULL, fake_out, 16, NULL),
+           TOPKP_ERR_PARAM_INVALID);
+    expect("sample_v2, empty batch",
+           topkp_sample_v2(NULL, 0, 8, 8, TOPKP_BF16, NULL, NULL, NULL, NULL, 8, 0.0f, 64, 1, NULL, 8, fake_tok, NULL,
+                           NULL, NULL, 0, NULL),
+           TOPKP_SUCCESS);
+    if (topkp_sample_v2_workspace_size(2, 8, TOPKP_BF16) == 0) {
+      printf("FAIL: sample_v2 workspace size is 0\n");
+      ++failures;
+    }
+  }
   if (failures == 0) printf("abi ok\n");
   return failures == 0 ? 0 : 1;
 }

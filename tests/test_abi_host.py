@@ -22,13 +22,14 @@ def lib():
 def _declared():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(topkp_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(topkp_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_expected_calls():
-    assert _declared() == sorted(["topkp_apply", "topkp_apply_sorted", "topkp_sample", "topkp_sort",
-                                  "topkp_sort_workspace_size", "topkp_sort_static", "topkp_last_error_string",
-                                  "topkp_device_status", "topkp_last_launch_count"])
+    assert _declared() == sorted(["topkp_apply", "topkp_apply_sorted", "topkp_sample", "topkp_sample_v2",
+                                  "topkp_sample_v2_workspace_size", "topkp_sort", "topkp_sort_workspace_size",
+                                  "topkp_sort_static", "topkp_last_error_string", "topkp_device_status",
+                                  "topkp_last_launch_count"])
 
 
 def test_every_declared_symbol_is_exported(lib):

@@ -174,6 +174,55 @@ def sample(filtered, min_p=None, q=None, eps: float = 1e-10, out=None, want_out:
     return token, out
 
 
+def sample_v2(logits, k=None, p=None, min_p=None, q=None, eps: float = 1e-10, ks_max: int = 1024,
+              input_is_logits: bool = True, need_sample_result: bool = False, workspace=None):
+    """The TopKTopPSampleV2 semantics (topkp_sample_v2) on a [B, V] CUDA tensor.
+
+    k: [B] int32; p, min_p: [B] float32; q: [B, V] float32 read by sorted
+    position; each optional.  With ``need_sample_result`` false returns
+    (token, select): token is [B] int32 (logitsSelectIdx), select the rows
+    in original order with removed elements -inf (0 for probability input,
+    logitsTopKPSelect).  Otherwise returns (logits_idx, sort_masked): [B, V]
+    int32 original indices of the sorted positions (-1 past the top-k
+    survivors) and [B, V] float32 masked probabilities."""
+    torch = _torch()
+    lib = _lib.load()
+    if not torch.is_tensor(logits) or logits.dim() != 2 or not logits.is_cuda:
+        raise ValueError("logits must be a 2-D CUDA tensor")
+    dt = _dtype_code(logits)
+    if logits.stride(1) != 1:
+        logits = logits.contiguous()
+    B, V = logits.shape
+    dev = logits.device
+    k = _vec(k, B, torch.int32, "k", dev)
+    p = _vec(p, B, torch.float32, "p", dev)
+    min_p = _vec(min_p, B, torch.float32, "min_p", dev)
+    if q is not None:
+        if not torch.is_tensor(q) or q.shape != (B, V) or q.dtype != torch.float32 or q.device != dev:
+            raise ValueError("q must be a float32 tensor shaped like logits on the same device")
+        if q.stride(1) != 1:
+            q = q.contiguous()
+    need = int(lib.topkp_sample_v2_workspace_size(B, V, dt))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if workspace.dtype != torch.uint8 or workspace.device != dev or workspace.numel() < need:
+        raise ValueError(f"workspace must be a uint8 tensor of at least {need} bytes on {dev}")
+    token = select = idx = sm = None
+    if need_sample_result:
+        idx = torch.empty((B, V), dtype=torch.int32, device=dev)
+        sm = torch.empty((B, V), dtype=torch.float32, device=dev)
+    else:
+        token = torch.empty(B, dtype=torch.int32, device=dev)
+        select = torch.empty((B, V), dtype=logits.dtype, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.topkp_sample_v2(_ptr(logits), B, V, logits.stride(0) if B > 1 else V, dt, _ptr(k), _ptr(p),
+                                   _ptr(min_p), _ptr(q), (q.stride(0) if B > 1 else V) if q is not None else V,
+                                   float(eps), int(ks_max), 1 if input_is_logits else 0, _ptr(select), V,
+                                   _ptr(token), _ptr(idx), _ptr(sm), _ptr(workspace), workspace.numel(),
+                                   _stream(dev)))
+    return (idx, sm) if need_sample_result else (token, select)
+
+
 def sort(logits, workspace=None):
     """The stable ascending sort of every row (topkp_sort): returns
     (sorted_value, sorted_indices), the inputs of ``apply_sorted``.

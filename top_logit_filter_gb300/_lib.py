@@ -22,8 +22,9 @@ TOPKP_ERR_NO_MEMORY = 561002
 TOPKP_MAX_V = 1 << 23
 
 # every entry point declared in include/topkp.h
-EXPORTS = ("topkp_apply", "topkp_apply_sorted", "topkp_sample", "topkp_sort", "topkp_sort_workspace_size",
-           "topkp_sort_static", "topkp_last_error_string", "topkp_device_status", "topkp_last_launch_count")
+EXPORTS = ("topkp_apply", "topkp_apply_sorted", "topkp_sample", "topkp_sample_v2", "topkp_sample_v2_workspace_size",
+           "topkp_sort", "topkp_sort_workspace_size", "topkp_sort_static", "topkp_last_error_string",
+           "topkp_device_status", "topkp_last_launch_count")
 
 _lib = None
 
@@ -43,6 +44,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topkp_apply_sorted.restype = c_int
     lib.topkp_sample.argtypes = [vp, i64, i64, i64, c_int, vp, vp, i64, ctypes.c_float, vp, i64, vp, vp]
     lib.topkp_sample.restype = c_int
+    lib.topkp_sample_v2_workspace_size.argtypes = [i64, i64, c_int]
+    lib.topkp_sample_v2_workspace_size.restype = ctypes.c_size_t
+    lib.topkp_sample_v2.argtypes = [vp, i64, i64, i64, c_int, vp, vp, vp, vp, i64, ctypes.c_float, ctypes.c_int32,
+                                    ctypes.c_int32, vp, i64, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.topkp_sample_v2.restype = c_int
     lib.topkp_sort_workspace_size.argtypes = [i64, i64, c_int]
     lib.topkp_sort_workspace_size.restype = ctypes.c_size_t
     lib.topkp_sort.argtypes = [vp, i64, i64, i64, c_int, vp, vp, vp, ctypes.c_size_t, vp]

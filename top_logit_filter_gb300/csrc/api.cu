@@ -65,6 +65,7 @@ int current_sms(int* dev_out) {
 }
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s for any single bounded wait
+constexpr int64_t kV2MaxV = 1LL << 20;          // [V2] Constraints: 0 < vocSize <= 2^20
 
 }  // namespace
 
@@ -412,6 +413,119 @@ topkp_status topkp_sort(const void* logits, int64_t B, int64_t V, int64_t ld_log
     ++launches;
   }
   g_last_launches = launches;
+  return TOPKP_SUCCESS;
+}
+
+size_t topkp_sample_v2_workspace_size(int64_t B, int64_t V, topkp_dtype dtype) {
+  const int es = esize_of(dtype);
+  if (!es || B <= 0 || V <= 0 || V > kV2MaxV) return 0;
+  const size_t n = (size_t)B * (size_t)V;
+  return (n * es + 255) / 256 * 256 + (n * 4 + 255) / 256 * 256 + topkp_sort_workspace_size(B, V, dtype);
+}
+
+topkp_status topkp_sample_v2(const void* logits, int64_t B, int64_t V, int64_t ld_logits, topkp_dtype dtype,
+                             const int32_t* top_k, const float* top_p, const float* min_p, const float* q,
+                             int64_t ldq, float eps, int32_t ks_max, int32_t input_is_logits, void* select,
+                             int64_t ld_select, int32_t* token, int32_t* logits_idx, float* sort_masked,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_launches = 0;
+  const int es = esize_of(dtype);
+  if (!es) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample_v2: unknown dtype %d", (int)dtype);
+  if (B < 0 || V < 0 || V > kV2MaxV)
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample_v2: bad shape B=%lld V=%lld (0 <= V <= 2^20)", (long long)B,
+                (long long)V);
+  if (ks_max < 1 || ks_max > 1024)
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample_v2: ks_max=%d outside [1, 1024]", (int)ks_max);
+  if (!(eps >= 0.0f)) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample_v2: eps must be >= 0");
+  if (!select && !token && !logits_idx && !sort_masked)
+    return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_sample_v2: no output given");
+  if (B == 0 || V == 0) return TOPKP_SUCCESS;
+  if (!logits) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_sample_v2: logits is NULL");
+  if (!workspace) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_sample_v2: workspace is NULL");
+  if (ld_logits < V || (select && ld_select < V) || (q && ldq < V))
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample_v2: a row stride is below V");
+  const size_t need = topkp_sample_v2_workspace_size(B, V, dtype);
+  if (workspace_bytes < need)
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample_v2: workspace of %zu bytes, %zu needed", workspace_bytes, need);
+  if ((uintptr_t)logits % es || (select && (uintptr_t)select % es) || (uintptr_t)workspace % 256 ||
+      (top_k && (uintptr_t)top_k % 4) || (top_p && (uintptr_t)top_p % 4) || (min_p && (uintptr_t)min_p % 4) ||
+      (q && (uintptr_t)q % 4) || (token && (uintptr_t)token % 4) || (logits_idx && (uintptr_t)logits_idx % 4) ||
+      (sort_masked && (uintptr_t)sort_masked % 4))
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample_v2: a pointer is not aligned (elements; workspace 256 bytes)");
+  const size_t n = (size_t)B * (size_t)V;
+  const size_t xb = (size_t)((B - 1) * ld_logits + V) * es;
+  const size_t sb = select ? (size_t)((B - 1) * ld_select + V) * es : 0;
+  const size_t qb = q ? (size_t)((B - 1) * ldq + V) * 4 : 0;
+  const void* outs[4] = {select, token, logits_idx, sort_masked};
+  const size_t osz[4] = {sb, (size_t)B * 4, n * 4, n * 4};
+  const void* ins[6] = {logits, top_k, top_p, min_p, q, workspace};
+  const size_t isz[6] = {xb, (size_t)B * 4, (size_t)B * 4, (size_t)B * 4, qb, need};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 6; ++j)
+      if (outs[i] && overlaps(outs[i], osz[i], ins[j], isz[j]))
+        return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample_v2: an output overlaps an input or the workspace");
+    for (int j = i + 1; j < 4; ++j)
+      if (outs[i] && outs[j] && overlaps(outs[i], osz[i], outs[j], osz[j]))
+        return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample_v2: two outputs overlap");
+  }
+  if (overlaps(workspace, need, logits, xb) || overlaps(workspace, need, q, qb))
+    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample_v2: the workspace overlaps an input");
+  int dev = 0;
+  if (current_sms(&dev) <= 0) return fail(TOPKP_ERR_LAUNCH, "topkp_sample_v2: no usable CUDA device");
+  if (B > INT_MAX) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sample_v2: B above 2^31 - 1");
+
+  // workspace: sorted values, their indices, then the sort's own scratch
+  char* w = (char*)workspace;
+  void* sv = w;
+  int32_t* si = reinterpret_cast<int32_t*>(w + (n * es + 255) / 256 * 256);
+  char* scratch = w + (n * es + 255) / 256 * 256 + (n * 4 + 255) / 256 * 256;
+  const int ks_aligned = (ks_max + 7) / 8 * 8 > 1024 ? 1024 : (ks_max + 7) / 8 * 8;
+
+  // 1. the rows whose top-k is skipped, sorted from the largest value down
+  SortArgs sa = {};
+  sa.x = logits;
+  sa.sorted_value = sv;
+  sa.sorted_indices = si;
+  sa.ws_index = reinterpret_cast<int32_t*>(scratch);
+  sa.ws_value = scratch + (n * 4 + 255) / 256 * 256;
+  sa.ldx = ld_logits;
+  sa.B = B;
+  sa.V = (int32_t)V;
+  sa.descending = 1;
+  sa.skip_k = top_k;
+  sa.skip_kmax = (int32_t)(V < ks_aligned ? V : ks_aligned);
+  cudaError_t e = launch_sort(dtype, sa, (cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(TOPKP_ERR_LAUNCH, "topkp_sample_v2: sort launch failed (%s)", cudaGetErrorString(e));
+  }
+  // 2. the filter stages and the sample
+  V2Args a = {};
+  a.x = logits;
+  a.ldx = ld_logits;
+  a.k = top_k;
+  a.p = top_p;
+  a.min_p = min_p;
+  a.q = q;
+  a.ldq = ldq;
+  a.eps = eps;
+  a.ks_aligned = ks_aligned;
+  a.input_is_logits = input_is_logits ? 1 : 0;
+  a.select = select;
+  a.ld_select = ld_select;
+  a.token = token;
+  a.logits_idx = logits_idx;
+  a.sort_masked = sort_masked;
+  a.sv = sv;
+  a.si = si;
+  a.B = B;
+  a.V = (int32_t)V;
+  e = launch_v2(dtype, a, (cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(TOPKP_ERR_LAUNCH, "topkp_sample_v2: launch failed (%s)", cudaGetErrorString(e));
+  }
+  g_last_launches = 3;
   return TOPKP_SUCCESS;
 }
 

@@ -119,9 +119,40 @@ struct SortArgs {
   int64_t ldx;
   int64_t B;
   int32_t V;
+  int32_t descending;       // largest first (equal values still in increasing index)
+  const int32_t* skip_k;    // [B] or nullptr: rows with 1 <= skip_k[row] <= skip_kmax are not sorted
+  int32_t skip_kmax;
 };
 
 cudaError_t launch_sort(topkp_dtype dt, const SortArgs& a, cudaStream_t s);
+
+// --------------------------------------------------------- sample (V2)
+// The TopKTopPSampleV2 semantics: rows whose top-k runs (1 <= k <=
+// min(V, ks_aligned)) are filtered by one CTA each without a full sort;
+// the other rows come sorted (descending) in sv / si.
+struct V2Args {
+  const void* x;            // logits [B, ldx]
+  int64_t ldx;
+  const int32_t* k;         // [B] or nullptr
+  const float* p;           // [B] or nullptr
+  const float* min_p;       // [B] or nullptr
+  const float* q;           // [B, ldq] or nullptr
+  int64_t ldq;
+  float eps;
+  int32_t ks_aligned;       // ks_max rounded up to a multiple of 8
+  int32_t input_is_logits;
+  void* select;             // [B, ld_select] dtype or nullptr
+  int64_t ld_select;
+  int32_t* token;           // [B] or nullptr
+  int32_t* logits_idx;      // [B, V] or nullptr
+  float* sort_masked;       // [B, V] or nullptr
+  const void* sv;           // [B, V] sorted values (rows whose top-k is skipped)
+  const int32_t* si;        // [B, V] their original indices
+  int64_t B;
+  int32_t V;
+};
+
+cudaError_t launch_v2(topkp_dtype dt, const V2Args& a, cudaStream_t s);
 
 // Error and launch reporting for entry points outside api.cu (the thread's
 // last error string, the last launch count), and the current device's SM

@@ -65,6 +65,13 @@ __global__ void __launch_bounds__(kThreads, 1) sort_kernel(const SortArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.x;
   const int V = a.V;
+  if (a.skip_k != nullptr) {
+    const int kv = a.skip_k[row];
+    if (kv >= 1 && kv <= a.skip_kmax) return;  // a row the caller does not need sorted
+  }
+  // descending: the keys inverted, so the stable ascending order of the
+  // inverted keys is the largest value first with ties in index order
+  const uint32_t kinv = a.descending ? (uint32_t)((1ull << D::kKeyBits) - 1ull) : 0u;
   const raw* xr = reinterpret_cast<const raw*>(a.x) + row * a.ldx;
   raw* out_v = reinterpret_cast<raw*>(a.sorted_value) + row * (int64_t)V;
   int32_t* out_i = a.sorted_indices + row * (int64_t)V;
@@ -82,7 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1) sort_kernel(const SortArgs a) {
     int32_t* di = to_out ? out_i : ws_i;
     const raw* sv = pass == 0 ? xr : (to_out ? ws_v : out_v);
     const int32_t* si = to_out ? ws_i : out_i;  // unused in pass 0
-    auto digit_of = [&](raw r) -> uint32_t { return (order_key<DT>(r) >> shift) & 255u; };
+    auto digit_of = [&](raw r) -> uint32_t { return ((order_key<DT>(r) ^ kinv) >> shift) & 255u; };
 
     // ---- 1. digit counts and bucket bases ----
     if (tid < kDigits) hist[tid] = 0;
