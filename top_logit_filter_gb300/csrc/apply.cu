@@ -70,6 +70,7 @@ constexpr int kSmallBins = 256;              // 8-bit digits over candidate list
 constexpr int kBPT = kBins / kThreads;       // 12-bit bins each thread scans
 constexpr int kKeyBlocks = (int)(kApplyBigBytes / (16 * 4));  // 16-key count blocks of the window path
 static_assert(kApplyAuxBytes >= (size_t)kKeyBlocks * (2 + 8), "block -> bucket map and block masses");
+static_assert(kApplyAuxBytes >= (size_t)kThreads * 8, "per-thread partial masses of a split mass table");
 static_assert(2 * kBins * 8 <= (int)kApplyBigBytes, "bucket mass bounds fit the big region");
 constexpr uint32_t kNoBlock = 0xffffffffu;   // bucket without a count block
 constexpr int kMassBins = (int)(kApplyBigBytes / 4);  // per-key counters of the bf16 mass-table path
@@ -346,9 +347,17 @@ __device__ __forceinline__ uint32_t block_first_true(uint32_t lo, uint32_t hi, P
 // last: the target reaches S (only the last sorted position survives).
 // Otherwise .bin is the cut key and .off the masked ties, or .bin = -1 when
 // the cut falls in a bin that ok(i) rejects.
-template <int DT, typename Cnt, typename KeyOf, typename Ok>
-__device__ __forceinline__ Sel mass_cut(int n, int first, Cnt cnt, KeyOf key_of, Ok ok, const MassRef& mr, float thr,
-                                        ApplyHdr& h, bool* last) {
+//
+// For a table split over a cluster (every CTA counted its own slice into
+// its own table, same layout), cnt reads this CTA's counts and cnt_all the
+// cluster's; part (kThreads words of shared scratch) carries each thread's
+// partial mass through one exchange, so only the walk to the cut reads the
+// peers' tables.  For a table already summed over the cluster, cnt_all is
+// cnt and part is null.
+template <int DT, typename Cnt, typename CntAll, typename KeyOf, typename Ok>
+__device__ __forceinline__ Sel mass_cut(int n, int first, Cnt cnt, CntAll cnt_all, KeyOf key_of, Ok ok,
+                                        const MassRef& mr, float thr, ApplyHdr& h, bool* last, const Clu& cl,
+                                        unsigned long long* part) {
   // an odd number of bins per thread: the lanes of a warp reading their
   // i-th bins then touch 32 different banks of a linear table
   const int bpt = ((n + kThreads - 1) / kThreads) | 1;
@@ -359,6 +368,11 @@ __device__ __forceinline__ Sel mass_cut(int n, int first, Cnt cnt, KeyOf key_of,
 #pragma unroll 4
   for (int i = i0; i < b1; ++i)
     s += (unsigned long long)cnt(i) * mass_fixed(value_of_key<DT>(key_of(i)), mr);
+  if (part != nullptr && cl.cs > 1) {
+    part[threadIdx.x] = s;
+    cl_merge<unsigned long long, 1>(cl, part, kThreads);
+    s = part[threadIdx.x];
+  }
   unsigned long long S;
   const unsigned long long ex = block_exclusive_scan(s, &S, h.ws);
   const unsigned long long target = mass_target(thr, S);
@@ -378,7 +392,7 @@ __device__ __forceinline__ Sel mass_cut(int n, int first, Cnt cnt, KeyOf key_of,
       unsigned long long u = 0, mk = 0;
       if (i < o1) {
         u = mass_fixed(value_of_key<DT>(key_of(i)), mr);
-        mk = (unsigned long long)cnt(i) * u;
+        mk = (unsigned long long)cnt_all(i) * u;
       }
       unsigned long long incl = mk;
 #pragma unroll
@@ -924,9 +938,10 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
         if (T < Lmax) continue;  // the lists may miss elements above the k-th largest
         if (topp) {
           bool last;
+          auto hcnt = [&](int i) { return hist[swz<kBPT>(i)]; };
           const Sel sp = mass_cut<DT>(
-              (int)(gmax - Lmin) + 1, bk, [&](int i) { return hist[swz<kBPT>(i)]; },
-              [&](int i) { return Lmin + (uint32_t)i; }, [](int) { return true; }, mr, thr, h, &last);
+              (int)(gmax - Lmin) + 1, bk, hcnt, hcnt, [&](int i) { return Lmin + (uint32_t)i; },
+              [](int) { return true; }, mr, thr, h, &last, cl, nullptr);
           if (last) {
             cut_last = true;
             r0 = hist[swz<kBPT>(gmax - Lmin)] - 1ull;
@@ -1079,8 +1094,9 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
       const bool shared_floor = lump && tfloor > 0;
       bool last;
       const Sel sp = mass_cut<DT>(
-          (int)gbin + 1, 0, [&](int v) { return cl_sum_at(cl, tab, v); }, key_of,
-          [&](int v) { return !(shared_floor && v == qn); }, mr, thr, h, &last);
+          (int)gbin + 1, 0, [&](int v) { return tab[v]; }, [&](int v) { return cl_sum_at(cl, tab, v); }, key_of,
+          [&](int v) { return !(shared_floor && v == qn); }, mr, thr, h, &last, cl,
+          reinterpret_cast<unsigned long long*>(aux));
       if (last) {
         cut_last = true;
         T = gmax;
