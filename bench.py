@@ -414,6 +414,136 @@ def run_sample(args):
 SAMPLE_SEED = 4242
 
 
+def _timed_steps(args, dev, stream, flush, call, prep=None):
+    """Seconds over args.steps calls of `call`, each after the L2 flush,
+    bracketed by CUDA events on the launching stream."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        if prep is not None:
+            prep()
+        flush.zero_()
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    return sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
+
+
+def run_fused(args):
+    """The filter and the sample in one pass (topkp_apply_sample) on the
+    B=256 x V=128256 bf16 joint batch, min_p ~ U[0.001, 0.2] and q ~ Exp(1):
+    one call per step, token only (the decode case) and with the output
+    row.  One JSON line (the token-only time is the headline)."""
+    import numpy as np
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import top_logit_filter_gb300 as tk
+    from rawutil import raw_to_torch
+    from top_logit_filter_gb300 import workloads
+
+    w = workloads.make(WORKLOAD)
+    B, V, dt = w["B"], w["V"], w["dtype"]
+    x = raw_to_torch(w["x"], dt, dev)
+    p = raw_to_torch(w["p"], dt, dev)
+    k = torch.from_numpy(w["k"]).to(dev)
+    rng = np.random.default_rng(SAMPLE_SEED)
+    q = torch.from_numpy(rng.exponential(1.0, size=(B, V)).astype(np.float32)).to(dev)
+    mp = torch.from_numpy(rng.uniform(0.001, 0.2, size=B).astype(np.float32)).to(dev)
+    out = torch.empty_like(x)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        tk.apply_sample(x, p=p, k=k, min_p=mp, q=q, want_out=False)
+        tk.apply_sample(x, p=p, k=k, min_p=mp, q=q, out=out)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(0) as clocks:
+        tok_s = _timed_steps(args, dev, stream, flush, lambda: tk.apply_sample(x, p=p, k=k, min_p=mp, q=q, want_out=False))
+    out_s = _timed_steps(args, dev, stream, flush, lambda: tk.apply_sample(x, p=p, k=k, min_p=mp, q=q, out=out))
+    two_s = _timed_steps(args, dev, stream, flush, lambda: tk.sample(tk.apply(x, p=p, k=k), min_p=mp, q=q,
+                                                                     want_out=False))
+    tk.device_status(dev)
+    peak, peak_kind = _peak_hbm()
+    alg_tok = B * V * 2        # the logits read; q is read only at the few survivors
+    line = {
+        "metric": "rows/s, fused top-k/top-p filter + min-p + sample (token only), B=256 V=128256 bf16",
+        "value": B * args.steps / tok_s, "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * tok_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "apply_sample_joint_B256_V128256_bf16", "B": B, "V": V,
+                   "min_p": "U[0.001, 0.2]", "q": "Exp(1) fp32",
+                   "ms_per_step_with_out": 1e3 * out_s / args.steps,
+                   "ms_per_step_two_calls_token_only": 1e3 * two_s / args.steps,
+                   "l2": "flushed before every timed step (512 MiB memset, outside the events)"},
+        "roofline": {"bound": "hbm", "achieved": alg_tok / (tok_s / args.steps) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": alg_tok / (tok_s / args.steps) / 1e9 / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} (copy bandwidth, burst)", "algorithmic_bytes_per_launch": alg_tok},
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_v2(args):
+    """The TopKTopPSampleV2 semantics (topkp_sample_v2) on a B=256 x
+    V=152064 bf16 decode batch (2*N(0,1) logits; k ~ U{1..1024}, 10% of the
+    rows 0 so top-k is skipped; p ~ U[0.5, 1]; min_p ~ U[0, 0.2]; q ~ Exp(1);
+    ks_max = 1024): one call per step, the token and the filtered row."""
+    import numpy as np
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import top_logit_filter_gb300 as tk
+    from rawutil import raw_to_torch, to_raw
+
+    rng = np.random.default_rng(SAMPLE_SEED + 1)
+    B, V = 256, 152064
+    x = raw_to_torch(to_raw((rng.standard_normal(B * V) * 2).astype(np.float32), "bf16").reshape(B, V), "bf16", dev)
+    kk = rng.integers(1, 1025, size=B).astype(np.int32)
+    kk[rng.random(B) < 0.1] = 0
+    k = torch.from_numpy(kk).to(dev)
+    p = torch.from_numpy(rng.uniform(0.5, 1.0, size=B).astype(np.float32)).to(dev)
+    mp = torch.from_numpy(rng.uniform(0.0, 0.2, size=B).astype(np.float32)).to(dev)
+    q = torch.from_numpy(rng.exponential(1.0, size=(B, V)).astype(np.float32)).to(dev)
+    ws = torch.empty(int(tk._lib.load().topkp_sample_v2_workspace_size(B, V, 2)), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    call = lambda: tk.sample_v2(x, k=k, p=p, min_p=mp, q=q, ks_max=1024, workspace=ws)
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(0) as clocks:
+        total_s = _timed_steps(args, dev, stream, flush, call)
+    tk.device_status(dev)
+    peak, peak_kind = _peak_hbm()
+    alg = B * V * 2 * 2
+    kernel_s = total_s / args.steps
+    line = {
+        "metric": "rows/s, TopKTopPSampleV2 semantics (token + filtered row), B=256 V=152064 bf16",
+        "value": B * args.steps / total_s, "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * kernel_s, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "sample_v2_B256_V152064_bf16", "B": B, "V": V, "ks_max": 1024,
+                   "rows_topk_skipped": int((kk == 0).sum()),
+                   "l2": "flushed before every timed step (512 MiB memset, outside the events)"},
+        "roofline": {"bound": "hbm", "achieved": alg / kernel_s / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": alg / kernel_s / 1e9 / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} (copy bandwidth, burst)", "algorithmic_bytes_per_launch": alg},
+        "gpu_launches": 3 * args.steps, "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_sort(args):
     """The stable sort (topkp_sort) of the pre-sorted workload's logits
     (B=512 x V=152064 bf16): one call per step after the same L2 flush, the
@@ -474,9 +604,10 @@ def main():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--op", choices=("filter", "sample", "sort"), default="filter",
+    ap.add_argument("--op", choices=("filter", "sample", "sort", "fused", "v2"), default="filter",
                     help="filter: the headline topkp_apply step; sample: the post-filter stage alone; "
-                         "sort: the stable sort alone")
+                         "sort: the stable sort alone; fused: filter + min-p + sample in one call; "
+                         "v2: the TopKTopPSampleV2 semantics")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing (profiling runs)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work for cpu_baseline")
     args = ap.parse_args()
@@ -488,6 +619,10 @@ def main():
         run_sample(args)
     elif args.op == "sort":
         run_sort(args)
+    elif args.op == "fused":
+        run_fused(args)
+    elif args.op == "v2":
+        run_v2(args)
     else:
         run_ours(args)
 

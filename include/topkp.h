@@ -113,6 +113,31 @@ topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_lo
                          void* out, int64_t ld_out, void* stream);
 
 /*
+ * topkp_apply_sample -- topkp_apply and topkp_sample in one pass: the filter
+ * of section 2 of the page, then, on its survivors, the min-p step and the
+ * sample of the web page "aclnnTopKTopPSampleV2" (Formula / minP sampling,
+ * Formula / Subsequent processing).  The result equals topkp_sample run on
+ * topkp_apply's output with the same min_p, q and eps (same arithmetic, so
+ * the same bits), but no filtered row is read back, and with out == NULL
+ * nothing is written but the token.
+ *
+ *   logits, B, V, ld_logits, dtype, p, k   as for topkp_apply.
+ *   min_p      device, [B] float, or NULL (no min-p).
+ *   q          device, [B, V] float, row stride ldq (>= V), or NULL (the
+ *              token is the largest element, of equals the largest index).
+ *   eps        added to every q, >= 0.
+ *   out        device, [B, V] of dtype, row stride ld_out (>= V), or NULL:
+ *              the rows after the filter and min-p.  out == logits with
+ *              ld_out == ld_logits (in place) is allowed.
+ *   token      device, [B] int32, or NULL.  out and token must not both be
+ *              NULL; neither may overlap another argument.
+ * Results: as topkp_apply and topkp_sample.  One kernel launch.
+ */
+topkp_status topkp_apply_sample(const void* logits, int64_t B, int64_t V, int64_t ld_logits, topkp_dtype dtype,
+                                const void* p, const int32_t* k, const float* min_p, const float* q, int64_t ldq,
+                                float eps, void* out, int64_t ld_out, int32_t* token, void* stream);
+
+/*
  * topkp_apply_sorted -- the graph op ApplyTopKTopPWithSorted (section 3 of
  * the page): the caller supplies each row already sorted.
  *

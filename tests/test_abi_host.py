@@ -26,7 +26,8 @@ def _declared():
 
 
 def test_header_declares_the_expected_calls():
-    assert _declared() == sorted(["topkp_apply", "topkp_apply_sorted", "topkp_sample", "topkp_sample_v2",
+    assert _declared() == sorted(["topkp_apply", "topkp_apply_sample", "topkp_apply_sorted", "topkp_sample",
+                                  "topkp_sample_v2",
                                   "topkp_sample_v2_workspace_size", "topkp_sort", "topkp_sort_workspace_size",
                                   "topkp_sort_static", "topkp_last_error_string", "topkp_device_status",
                                   "topkp_last_launch_count"])

@@ -103,6 +103,43 @@ def apply(logits, p=None, k=None, out=None):
     return out
 
 
+def apply_sample(logits, p=None, k=None, min_p=None, q=None, eps: float = 1e-10, out=None, want_out: bool = True):
+    """The filter and the sample in one pass (topkp_apply_sample): the same
+    result as ``sample(apply(logits, p, k), min_p, q, eps)``.  Returns
+    (token, out): token is [B] int32; out holds the rows after the filter and
+    min-p (``logits`` itself may be passed), or None when ``want_out`` is
+    false (then only the token is written)."""
+    torch = _torch()
+    lib = _lib.load()
+    if not torch.is_tensor(logits) or logits.dim() != 2 or not logits.is_cuda:
+        raise ValueError("logits must be a 2-D CUDA tensor")
+    dt = _dtype_code(logits)
+    if logits.stride(1) != 1:
+        logits = logits.contiguous()
+    B, V = logits.shape
+    dev = logits.device
+    p = _vec(p, B, logits.dtype, "p", dev)
+    k = _vec(k, B, torch.int32, "k", dev)
+    min_p = _vec(min_p, B, torch.float32, "min_p", dev)
+    if q is not None:
+        if not torch.is_tensor(q) or q.shape != (B, V) or q.dtype != torch.float32 or q.device != dev:
+            raise ValueError("q must be a float32 tensor shaped like logits on the same device")
+        if q.stride(1) != 1:
+            q = q.contiguous()
+    if want_out and out is None:
+        out = torch.empty((B, V), dtype=logits.dtype, device=dev)
+    if out is not None and (out.shape != (B, V) or out.dtype != logits.dtype or out.device != dev
+                            or out.stride(1) != 1):
+        raise ValueError("out must match logits in shape, dtype and device, with stride(1) == 1")
+    token = torch.empty(B, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.topkp_apply_sample(_ptr(logits), B, V, logits.stride(0) if B > 1 else V, dt, _ptr(p), _ptr(k),
+                                      _ptr(min_p), _ptr(q), (q.stride(0) if B > 1 else V) if q is not None else V,
+                                      float(eps), _ptr(out), (out.stride(0) if B > 1 else V) if out is not None else V,
+                                      _ptr(token), _stream(dev)))
+    return token, out
+
+
 def apply_sorted(sorted_value, sorted_indices, p=None, k=None, logits=None, out=None):
     """ApplyTopKTopPWithSorted: filter pre-sorted rows.
 

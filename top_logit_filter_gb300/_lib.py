@@ -22,7 +22,7 @@ TOPKP_ERR_NO_MEMORY = 561002
 TOPKP_MAX_V = 1 << 23
 
 # every entry point declared in include/topkp.h
-EXPORTS = ("topkp_apply", "topkp_apply_sorted", "topkp_sample", "topkp_sample_v2", "topkp_sample_v2_workspace_size",
+EXPORTS = ("topkp_apply", "topkp_apply_sample", "topkp_apply_sorted", "topkp_sample", "topkp_sample_v2", "topkp_sample_v2_workspace_size",
            "topkp_sort", "topkp_sort_workspace_size", "topkp_sort_static", "topkp_last_error_string",
            "topkp_device_status", "topkp_last_launch_count")
 
@@ -40,6 +40,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, i64, i32p, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
     lib.topkp_apply.argtypes = [vp, i64, i64, i64, c_int, vp, i32p, vp, i64, vp]
     lib.topkp_apply.restype = c_int
+    lib.topkp_apply_sample.argtypes = [vp, i64, i64, i64, c_int, vp, i32p, vp, vp, i64, ctypes.c_float, vp, i64, vp,
+                                       vp]
+    lib.topkp_apply_sample.restype = c_int
     lib.topkp_apply_sorted.argtypes = [vp, i32p, i64, i64, c_int, vp, i32p, vp, vp, vp]
     lib.topkp_apply_sorted.restype = c_int
     lib.topkp_sample.argtypes = [vp, i64, i64, i64, c_int, vp, vp, i64, ctypes.c_float, vp, i64, vp, vp]

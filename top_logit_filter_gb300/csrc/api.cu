@@ -154,45 +154,69 @@ const char* topkp_last_error_string(void) { return g_last_error.c_str(); }
 
 int topkp_last_launch_count(void) { return g_last_launches; }
 
-topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_logits, topkp_dtype dtype,
-                         const void* p, const int32_t* k, void* out, int64_t ld_out, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// topkp_apply and topkp_apply_sample: the same checks and launch; the fused
+// call adds min-p and the sample, and may leave out NULL (token only).
+topkp_status apply_impl(const char* fn, const void* logits, int64_t B, int64_t V, int64_t ld_logits,
+                        topkp_dtype dtype, const void* p, const int32_t* k, bool fused, const float* min_p,
+                        const float* q, int64_t ldq, float eps, void* out, int64_t ld_out, int32_t* token,
+                        void* stream) {
   g_last_launches = 0;
-  if (!p && !k) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_apply: p and k are both NULL (at least one is required)");
+  if (!p && !k) return fail(TOPKP_ERR_PARAM_NULLPTR, "%s: p and k are both NULL (at least one is required)", fn);
+  if (fused && !out && !token) return fail(TOPKP_ERR_PARAM_NULLPTR, "%s: out and token are both NULL", fn);
   const int es = esize_of(dtype);
-  if (!es) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: unknown dtype %d", (int)dtype);
-  if (B < 0 || V < 0) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: negative shape B=%lld V=%lld", (long long)B, (long long)V);
-  if (V > TOPKP_MAX_V) return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: V=%lld exceeds the maximum %lld", (long long)V, (long long)TOPKP_MAX_V);
+  if (!es) return fail(TOPKP_ERR_PARAM_INVALID, "%s: unknown dtype %d", fn, (int)dtype);
+  if (B < 0 || V < 0) return fail(TOPKP_ERR_PARAM_INVALID, "%s: negative shape B=%lld V=%lld", fn, (long long)B, (long long)V);
+  if (V > TOPKP_MAX_V)
+    return fail(TOPKP_ERR_PARAM_INVALID, "%s: V=%lld exceeds the maximum %lld", fn, (long long)V, (long long)TOPKP_MAX_V);
+  if (fused && !(eps >= 0.0f)) return fail(TOPKP_ERR_PARAM_INVALID, "%s: eps must be >= 0", fn);
   if (B == 0 || V == 0) return TOPKP_SUCCESS;
-  if (!logits) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_apply: logits is NULL");
-  if (!out) return fail(TOPKP_ERR_PARAM_NULLPTR, "topkp_apply: out is NULL");
-  if (ld_logits < V || ld_out < V)
-    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: row stride below V (ld_logits=%lld ld_out=%lld V=%lld)",
+  if (!logits) return fail(TOPKP_ERR_PARAM_NULLPTR, "%s: logits is NULL", fn);
+  if (!out && !fused) return fail(TOPKP_ERR_PARAM_NULLPTR, "%s: out is NULL", fn);
+  if (ld_logits < V || (out && ld_out < V) || (q && ldq < V))
+    return fail(TOPKP_ERR_PARAM_INVALID, "%s: row stride below V (ld_logits=%lld ld_out=%lld V=%lld)", fn,
                 (long long)ld_logits, (long long)ld_out, (long long)V);
-  if ((uintptr_t)logits % es || (uintptr_t)out % es || (p && (uintptr_t)p % es) || (k && (uintptr_t)k % 4))
-    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: a pointer is not aligned to its element size");
+  if ((uintptr_t)logits % es || (out && (uintptr_t)out % es) || (p && (uintptr_t)p % es) || (k && (uintptr_t)k % 4) ||
+      (min_p && (uintptr_t)min_p % 4) || (q && (uintptr_t)q % 4) || (token && (uintptr_t)token % 4))
+    return fail(TOPKP_ERR_PARAM_INVALID, "%s: a pointer is not aligned to its element size", fn);
   const size_t xbytes = (size_t)((B - 1) * ld_logits + V) * es;
-  const size_t obytes = (size_t)((B - 1) * ld_out + V) * es;
+  const size_t obytes = out ? (size_t)((B - 1) * ld_out + V) * es : 0;
+  const size_t qbytes = q ? (size_t)((B - 1) * ldq + V) * 4 : 0;
   const bool in_place = (logits == out && ld_logits == ld_out);
-  if (!in_place && overlaps(logits, xbytes, out, obytes))
-    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: out partially overlaps logits");
-  if (overlaps(p, (size_t)B * es, out, obytes) || overlaps(k, (size_t)B * 4, out, obytes))
-    return fail(TOPKP_ERR_PARAM_INVALID, "topkp_apply: out overlaps p or k");
+  if (out && !in_place && overlaps(logits, xbytes, out, obytes))
+    return fail(TOPKP_ERR_PARAM_INVALID, "%s: out partially overlaps logits", fn);
+  if (overlaps(p, (size_t)B * es, out, obytes) || overlaps(k, (size_t)B * 4, out, obytes) ||
+      overlaps(min_p, (size_t)B * 4, out, obytes) || overlaps(q, qbytes, out, obytes))
+    return fail(TOPKP_ERR_PARAM_INVALID, "%s: out overlaps another argument", fn);
+  if (token && (overlaps(token, (size_t)B * 4, logits, xbytes) || overlaps(token, (size_t)B * 4, out, obytes) ||
+                overlaps(token, (size_t)B * 4, p, (size_t)B * es) || overlaps(token, (size_t)B * 4, k, (size_t)B * 4) ||
+                overlaps(token, (size_t)B * 4, min_p, (size_t)B * 4) || overlaps(token, (size_t)B * 4, q, qbytes)))
+    return fail(TOPKP_ERR_PARAM_INVALID, "%s: token overlaps another argument", fn);
 
   int dev = 0;
   const int sms = current_sms(&dev);
-  if (sms <= 0) return fail(TOPKP_ERR_LAUNCH, "topkp_apply: no usable CUDA device");
+  if (sms <= 0) return fail(TOPKP_ERR_LAUNCH, "%s: no usable CUDA device", fn);
   ApplyArgs a = {};
   a.x = logits;
   a.out = out;
   a.p = p;
   a.k = k;
   a.ldx = ld_logits;
-  a.ldo = ld_out;
+  a.ldo = out ? ld_out : V;
   a.V = (int32_t)V;
   const ApplyPlan plan = plan_apply(B, V, k != nullptr, sms, getenv("TOPKP_FORCE_PLAN"));
   a.cs = plan.cs;
   a.mixed = plan.mixed;
   a.force = plan.force_bits;
+  a.fused = fused ? 1 : 0;
+  a.min_p = min_p;
+  a.q = q;
+  a.ldq = q ? ldq : V;
+  a.eps = eps;
+  a.token = token;
   // cs CTAs per row; grid.x must stay below 2^31
   const int64_t max_rows = INT_MAX / a.cs;
   int launches = 0;
@@ -201,19 +225,39 @@ topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_lo
     ApplyArgs ai = a;
     ai.B = nb;
     ai.x = (const char*)logits + r0 * ld_logits * es;
-    ai.out = (char*)out + r0 * ld_out * es;
+    ai.out = out ? (char*)out + r0 * ld_out * es : nullptr;
     ai.p = p ? (const char*)p + r0 * es : nullptr;
     ai.k = k ? k + r0 : nullptr;
+    ai.min_p = min_p ? min_p + r0 : nullptr;
+    ai.q = q ? q + r0 * ldq : nullptr;
+    ai.token = token ? token + r0 : nullptr;
     const cudaError_t e = launch_apply(dtype, ai, (cudaStream_t)stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
-      return fail(TOPKP_ERR_LAUNCH, "topkp_apply: launch failed (%s; cs=%d smem=%zu)", cudaGetErrorString(e), a.cs,
+      return fail(TOPKP_ERR_LAUNCH, "%s: launch failed (%s; cs=%d smem=%zu)", fn, cudaGetErrorString(e), a.cs,
                   kApplySmem);
     }
     ++launches;
   }
   g_last_launches = launches;
   return TOPKP_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_logits, topkp_dtype dtype,
+                         const void* p, const int32_t* k, void* out, int64_t ld_out, void* stream) {
+  return apply_impl("topkp_apply", logits, B, V, ld_logits, dtype, p, k, false, nullptr, nullptr, 0, 0.0f, out,
+                    ld_out, nullptr, stream);
+}
+
+topkp_status topkp_apply_sample(const void* logits, int64_t B, int64_t V, int64_t ld_logits, topkp_dtype dtype,
+                                const void* p, const int32_t* k, const float* min_p, const float* q, int64_t ldq,
+                                float eps, void* out, int64_t ld_out, int32_t* token, void* stream) {
+  return apply_impl("topkp_apply_sample", logits, B, V, ld_logits, dtype, p, k, true, min_p, q, ldq, eps, out,
+                    ld_out, token, stream);
 }
 
 topkp_status topkp_apply_sorted(const void* sorted_value, const int32_t* sorted_indices, int64_t B, int64_t V,

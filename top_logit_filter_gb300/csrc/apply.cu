@@ -480,7 +480,7 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
   int cph = 0;  // cluster exchange phase (cluster.cuh)
   const int V = a.V;
   const raw* xr = reinterpret_cast<const raw*>(a.x) + row * a.ldx;
-  raw* orow = reinterpret_cast<raw*>(a.out) + row * a.ldo;
+  raw* orow = a.out ? reinterpret_cast<raw*>(a.out) + row * a.ldo : nullptr;  // nullptr: token only
   ckey* seg = reinterpret_cast<ckey*>(big) + warp * CAPW;
   uint32_t* segi = reinterpret_cast<uint32_t*>(big + (size_t)kWarps * CAPW * sizeof(ckey)) + warp * CAPW;
   unsigned long long* mass = reinterpret_cast<unsigned long long*>(big);
@@ -497,7 +497,7 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
   const bool window = !topk && topp && !p_zero && KB == 16 && !generic_only;
   const bool masstab = window && DT == TOPKP_BF16;
   const bool in_place = reinterpret_cast<const void*>(xr) == reinterpret_cast<const void*>(orow);
-  if (keepall && in_place) return;  // nothing to filter, nothing to move
+  if (keepall && in_place && !a.fused) return;  // nothing to filter, nothing to move
 
   // ---- row geometry: unaligned head, whole 16-byte vectors, tail ----
   const uintptr_t xaddr = reinterpret_cast<uintptr_t>(xr);
@@ -808,7 +808,9 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
         }
       });
     }
-  } else if (!keepall) {
+  } else if (!keepall || a.fused) {
+    // the max alone (rows filtered by the max's threshold; and every row of
+    // the fused sample, whose min-p and race are relative to the max)
     sweep(Loads<kLoadsSimple>{}, ReadAs<kReadNc>{}, [&](int, const uint4& q, int nv) {
       if (nv) kmax = max(kmax, vmax_key(q));
     });
@@ -825,7 +827,7 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
   // the write then waits for them and scatters the survivors.
   constexpr int kFillBlock = 8192;
   static_assert(kFillBlock <= (int)kApplyAuxBytes, "fill block fits the aux region");
-  const bool early_fill = topk && !generic_only && kv <= V / 8 &&
+  const bool early_fill = topk && !generic_only && kv <= V / 8 && orow != nullptr &&
                           reinterpret_cast<const void*>(orow) != reinterpret_cast<const void*>(xr);
   if (early_fill) {
     uint4* negs = reinterpret_cast<uint4*>(aux);
@@ -1453,6 +1455,204 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
       fence_proxy_async_global();
     }
     __syncthreads();
+  }
+
+  // ---- fused sample: min-p and the exponential race on the survivors ----
+  // The steps of the page aclnnTopKTopPSampleV2 (Formula / minP sampling,
+  // Subsequent processing) on the filter's survivors, with the arithmetic of
+  // topkp_sample: with t = (x - max) log2 e, min-p keeps t >= log2(min_p)
+  // (min_p >= 1: the last sorted position alone); QSample takes the largest
+  // t - log2(q + eps), ties to the larger index; without q the token is the
+  // last sorted position (the largest value, of equals the largest index),
+  // which every row keeps.  out, when given, holds the rows after min-p.
+  if (a.fused) {
+    const float mpv = a.min_p ? a.min_p[row] : 0.0f;
+    const bool minp_on = mpv > 0.0f;
+    const bool only_last = mpv >= 1.0f;
+    const float* qr = a.q ? a.q + row * a.ldq : nullptr;
+    const bool race_on = qr != nullptr && !only_last && a.token != nullptr;
+    const float nml = -value_of_key<DT>(gmax) * 1.4426950408889634f;
+    const float lmp = minp_on ? log2f(mpv) : -INFINITY;
+    float bsc = -INFINITY;
+    int bidx = -1;
+    unsigned long long lastp = 0;  // largest (key << 32 | position): the last sorted position
+    auto see_last = [&](raw r, int i) {
+      const unsigned long long pk = ((unsigned long long)order_key<DT>(r) << 32) | (uint32_t)i;
+      lastp = pk > lastp ? pk : lastp;
+    };
+    // a survivor of the filter: whether min-p keeps it, racing it if so
+    auto keep_race = [&](raw r, int i) -> bool {
+      const float t = fmaf(D::to_float(r), 1.4426950408889634f, nml);
+      if (!(t >= lmp)) return false;
+      if (race_on) {
+        const float sc = t - __log2f(__ldg(qr + i) + a.eps);
+        if (sc > bsc || (sc == bsc && i > bidx)) {
+          bsc = sc;
+          bidx = i;
+        }
+      }
+      return true;
+    };
+    const int myn = h.fill ? (int)h.nseg[warp] : 0;
+    const uint32_t tcut = h.tie_cut;
+    auto listed_survivor = [&](int j) -> bool {
+      const uint32_t key = order_key<DT>((raw)seg[j]);
+      return key > T || (key == T && segi[j] >= tcut);
+    };
+    // this CTA's slice of the output row filled with -inf (rows whose
+    // survivors are listed; the early fill did it already)
+    auto fill_slice = [&]() {
+      raw* ob = orow + e0;
+      const int n = e1 - e0;
+      const uintptr_t oaddr = reinterpret_cast<uintptr_t>(ob);
+      const int ohead = min(n, (int)(((16u - (uint32_t)(oaddr & 15u)) & 15u) / (uint32_t)sizeof(raw)));
+      const int onv = (n - ohead) / VEC;
+      for (int i = tid; i < ohead; i += kThreads) ob[i] = D::kNegInf;
+      uint4* ov = reinterpret_cast<uint4*>(ob + ohead);
+      for (int i = tid; i < onv; i += kThreads) st_global_hint(ov + i, make_uint4(NEG2, NEG2, NEG2, NEG2), pol_first);
+      for (int i = ohead + onv * VEC + tid; i < n; i += kThreads) ob[i] = D::kNegInf;
+    };
+    // the filter's keep rule per vector for rows that are not listed: the
+    // per-warp tie counts of T, counted here when the cut did not provide them
+    int rule = kKeepAll;
+    unsigned long long seen = 0;
+    if (!h.fill && !keepall) {
+      if (!(r0_known && (r0 == 0 || have_wtie))) {
+        uint32_t wn = 0;  // warp-uniform
+        sweep(Loads<kLoadsSimple>{}, ReadAs<kReadCg>{}, [&](int, const uint4& q, int nv) {
+          wn += __reduce_add_sync(0xffffffffu, (uint32_t)__popc(eq_bits(q, nv, T2)));
+        });
+        if (lane == 0) h.wtie[warp] = wn;
+        __syncthreads();
+        unsigned long long all_mine = 0;
+        for (int w = 0; w < kWarps; ++w) all_mine += h.wtie[w];
+        const unsigned long long v1[1] = {all_mine};
+        unsigned long long ex1[1], tot1[1];
+        cl_prefix<1>(cl, h.cx, cph, v1, ex1, tot1);
+        tie_off = ex1[0];
+        if (!r0_known) r0 = tot1[0] - 1ull;  // only the last sorted position survives
+      }
+      if (r0 == 0) {
+        rule = kTiesKept;
+      } else {
+        unsigned long long pre = tie_off;
+        for (int w = 0; w < warp; ++w) pre += h.wtie[w];
+        const unsigned long long mine = h.wtie[warp];
+        rule = (pre + mine <= r0) ? kTiesMasked : (pre >= r0 ? kTiesKept : kTiesStraddle);
+        seen = pre;
+      }
+    }
+    // bit j set when element j of the vector survives the filter
+    auto survivor_bits = [&](const uint4& qin, int nv) -> uint32_t {
+      uint32_t keep_ties = 0;
+      if (rule == kTiesStraddle) {
+        uint32_t tb = eq_bits(qin, nv, T2);
+        const uint32_t cnt = __popc(tb);
+        if (__any_sync(0xffffffffu, cnt != 0)) {
+          const uint32_t incl = warp_incl_scan(cnt);
+          unsigned long long rank = seen + incl - cnt;
+          while (tb) {
+            const int j = __ffs(tb) - 1;
+            tb &= tb - 1;
+            if (rank >= r0) keep_ties |= 1u << j;
+            ++rank;
+          }
+          seen += __shfl_sync(0xffffffffu, incl, 31);
+        }
+      }
+      const uint32_t valid = (1u << nv) - 1u;
+      if (rule == kKeepAll) return valid;
+      uint32_t b;
+      if (rule == kTiesKept) b = ge_bits(qin, nv, T2);
+      else b = mask_bits<KB>(P::gt(qin.x, T2), P::gt(qin.y, T2), P::gt(qin.z, T2), P::gt(qin.w, T2)) | keep_ties;
+      return b & valid;
+    };
+    // one vector written with the elements of `bits` kept, -inf elsewhere
+    auto write_vec = [&](int e, const uint4& qin, int nv, uint32_t bits) {
+      uint4 q = qin;
+      q.x = (q.x & bits_word_mask<KB>(bits, 0)) | (NEG2 & ~bits_word_mask<KB>(bits, 0));
+      q.y = (q.y & bits_word_mask<KB>(bits, 1)) | (NEG2 & ~bits_word_mask<KB>(bits, 1));
+      q.z = (q.z & bits_word_mask<KB>(bits, 2)) | (NEG2 & ~bits_word_mask<KB>(bits, 2));
+      q.w = (q.w & bits_word_mask<KB>(bits, 3)) | (NEG2 & ~bits_word_mask<KB>(bits, 3));
+      if (nv == VEC && vec_out) {
+        st_global_hint(orow + e, q, pol_first);
+      } else {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+          if (j < nv) orow[e + j] = vec_elem<DT>(q, j);
+      }
+    };
+
+    if (only_last) {
+      // the last sorted position alone stays: find it, then write it
+      if (h.fill) {
+        for (int j = lane; j < myn; j += 32) see_last((raw)seg[j], (int)segi[j]);
+      } else {
+        sweep(Loads<kLoadsSimple>{}, ReadAs<kReadCg>{}, [&](int e, const uint4& q, int nv) {
+#pragma unroll
+          for (int j = 0; j < VEC; ++j)
+            if (j < nv) see_last(vec_elem<DT>(q, j), e + j);
+        });
+      }
+      lastp = cl_reduce1<kClMax>(cl, h.cx, cph, block_max_u64(lastp, h.ws));
+      const int last = (int)(uint32_t)lastp;
+      if (orow) {
+        if (h.fill) {
+          if (!early_fill) fill_slice();
+          __syncthreads();
+          for (int j = lane; j < myn; j += 32)
+            if ((int)segi[j] == last) orow[last] = (raw)seg[j];
+        } else {
+          sweep(Loads<kLoadsSimple>{}, ReadAs<kReadLast>{}, [&](int e, const uint4& q, int nv) {
+            if (nv == 0) return;
+            const uint32_t bits = (last >= e && last < e + nv) ? 1u << (last - e) : 0u;
+            write_vec(e, q, nv, bits);
+          });
+        }
+      }
+      if (a.token && tid == 0 && cl.rank == 0) a.token[row] = last;
+      return;
+    }
+
+    if (h.fill) {
+      if (orow && !early_fill) {
+        fill_slice();
+        __syncthreads();
+      }
+      for (int j = lane; j < myn; j += 32) {
+        if (!listed_survivor(j)) continue;
+        const raw r = (raw)seg[j];
+        const int i = (int)segi[j];
+        see_last(r, i);
+        if (keep_race(r, i) && orow) orow[i] = r;
+      }
+    } else {
+      sweep(Loads<kLoadsSimple>{}, ReadAs<kReadLast>{}, [&](int e, const uint4& qin, int nv) {
+        const uint32_t sb = survivor_bits(qin, nv);
+        if (nv == 0) return;
+        uint32_t kb = 0;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+          if ((sb >> j) & 1u) {
+            const raw r = vec_elem<DT>(qin, j);
+            see_last(r, e + j);
+            if (keep_race(r, e + j)) kb |= 1u << j;
+          }
+        }
+        if (orow) write_vec(e, qin, nv, kb);
+      });
+    }
+    if (a.token) {
+      unsigned long long pick;
+      if (race_on) {
+        pick = bidx < 0 ? 0ull : (((unsigned long long)float_order_key(bsc) << 32) | (uint32_t)bidx);
+        pick = cl_reduce1<kClMax>(cl, h.cx, cph, block_max_u64(pick, h.ws));
+      } else {
+        pick = cl_reduce1<kClMax>(cl, h.cx, cph, block_max_u64(lastp, h.ws));
+      }
+      if (tid == 0 && cl.rank == 0) a.token[row] = (int)(uint32_t)pick;
+    }
+    return;
   }
 
   // ---- write: the listed survivors over a -inf row ([guide] §2 step 8) ----

@@ -428,6 +428,33 @@ __device__ __forceinline__ void block_exclusive_scan2(unsigned long long a, unsi
   __syncthreads();
 }
 
+// Largest 64-bit value over the CTA (every thread gets it).  ws: kWarps
+// words of shared scratch.  Contains __syncthreads().
+__device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* ws) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w > v ? w : v;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();  // ws may still be read from an earlier call
+  if (lane == 0) ws[warp] = v;
+  __syncthreads();
+  v = ws[lane < kWarps ? lane : 0];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+// An fp32 score as an unsigned key of the same order (for packed maxima).
+__device__ __forceinline__ uint32_t float_order_key(float f) {
+  const uint32_t fb = __float_as_uint(f);
+  return (fb & 0x80000000u) ? ~fb : (fb | 0x80000000u);
+}
+
 __device__ __forceinline__ unsigned long long block_sum(unsigned long long v, unsigned long long* ws) {
   unsigned long long t;
   block_exclusive_scan(v, &t, ws);

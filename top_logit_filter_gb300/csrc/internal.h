@@ -25,6 +25,14 @@ struct ApplyArgs {
   int32_t cs;             // CTAs per cluster (1, 2, 4 or 8)
   int32_t mixed;          // clusters take one row without top-k, or cs rows with top-k (one per CTA)
   int32_t force;          // kApplyForce* bits (testing: route rows to one path)
+  // fused sample (topkp_apply_sample): min-p and the exponential race on the
+  // filter's survivors; out may then be nullptr (token only)
+  int32_t fused;
+  const float* min_p;     // [B] or nullptr
+  const float* q;         // [B, ldq] or nullptr
+  int64_t ldq;
+  float eps;
+  int32_t* token;         // [B] or nullptr
 };
 
 // Every row that needs a cut takes the generic radix path.

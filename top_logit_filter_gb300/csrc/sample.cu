@@ -28,26 +28,6 @@ namespace topkp {
 
 namespace {
 
-// Largest 64-bit value over the CTA (every thread gets it).
-__device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* ws) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
-    v = w > v ? w : v;
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();  // ws may still be read from an earlier call
-  if (lane == 0) ws[warp] = v;
-  __syncthreads();
-  v = ws[lane < kWarps ? lane : 0];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
-    v = w > v ? w : v;
-  }
-  return v;
-}
-
 // 16 bytes through the non-coherent path, not allocated in L1.
 __device__ __forceinline__ uint4 ld_stream_v4(const uint4* p) {
   uint4 v;
@@ -375,8 +355,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleArgs a)
   if (a.token) {
     if (qr) {
       // float order as unsigned order, then the larger index among equals
-      const uint32_t fb = __float_as_uint(bsc);
-      const uint32_t key = (fb & 0x80000000u) ? ~fb : (fb | 0x80000000u);
+      const uint32_t key = float_order_key(bsc);
       unsigned long long race = bidx < 0 ? 0ull : (((unsigned long long)key << 32) | (uint32_t)bidx);
       race = block_max_u64(race, ws);
       if (tid == 0) a.token[row] = (int)(uint32_t)race;
