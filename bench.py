@@ -77,7 +77,7 @@ def _kernel_hash():
     kernels do not change it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "top_logit_filter_gb300", "csrc")
-    for name in ("apply.cu", "common.cuh"):
+    for name in ("apply.cu", "common.cuh", "cluster.cuh"):
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

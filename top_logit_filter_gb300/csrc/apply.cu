@@ -97,6 +97,7 @@ struct __align__(16) ApplyHdr {
   int mt_qn;                             // mag clamped to >= floor; qn = bin of the negative floor;
   uint32_t mt_lump;                      // k0 = provisional max key; lump: floors hold zero-equal keys
   uint32_t slot;                         // block_first_true scratch
+  uint32_t rcount;                       // fused sample: race candidates listed
   ClSlots cx;                            // cluster exchange slots (rows split over a cluster)
 };
 static_assert(sizeof(ApplyHdr) <= kApplyHdrBytes, "header too large");
@@ -1480,19 +1481,28 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
       const unsigned long long pk = ((unsigned long long)order_key<DT>(r) << 32) | (uint32_t)i;
       lastp = pk > lastp ? pk : lastp;
     };
+    auto t_of = [&](raw r) -> float { return fmaf(D::to_float(r), 1.4426950408889634f, nml); };
+    // one race candidate (score t - log2(q + eps), ties to the larger index)
+    auto race = [&](float t, float qv, int i) {
+      const float sc = t - __log2f(qv + a.eps);
+      if (sc > bsc || (sc == bsc && i > bidx)) {
+        bsc = sc;
+        bidx = i;
+      }
+    };
     // a survivor of the filter: whether min-p keeps it, racing it if so
     auto keep_race = [&](raw r, int i) -> bool {
-      const float t = fmaf(D::to_float(r), 1.4426950408889634f, nml);
+      const float t = t_of(r);
       if (!(t >= lmp)) return false;
-      if (race_on) {
-        const float sc = t - __log2f(__ldg(qr + i) + a.eps);
-        if (sc > bsc || (sc == bsc && i > bidx)) {
-          bsc = sc;
-          bidx = i;
-        }
-      }
+      if (race_on) race(t, __ldg(qr + i), i);
       return true;
     };
+    // race candidates of the rows that are not listed: (position, t) pairs
+    // in the 64 KB region, free once the cut is known; raced four per thread
+    // at a time after the write sweep so that their q loads overlap
+    constexpr int kRaceCap = (int)(kApplyBigBytes / 8);
+    uint32_t* rpos = reinterpret_cast<uint32_t*>(big);
+    float* rt = reinterpret_cast<float*>(big + kApplyBigBytes / 2);
     const int myn = h.fill ? (int)h.nseg[warp] : 0;
     const uint32_t tcut = h.tie_cut;
     auto listed_survivor = [&](int j) -> bool {
@@ -1542,6 +1552,7 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
         seen = pre;
       }
     }
+    const unsigned long long seen0 = seen;  // a second sweep ranks the ties from the start again
     // bit j set when element j of the vector survives the filter
     auto survivor_bits = [&](const uint4& qin, int nv) -> uint32_t {
       uint32_t keep_ties = 0;
@@ -1619,28 +1630,103 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
         fill_slice();
         __syncthreads();
       }
-      for (int j = lane; j < myn; j += 32) {
-        if (!listed_survivor(j)) continue;
-        const raw r = (raw)seg[j];
-        const int i = (int)segi[j];
-        see_last(r, i);
-        if (keep_race(r, i) && orow) orow[i] = r;
+      // the listed survivors, four per lane at a time so their q loads overlap
+      for (int j0 = lane; j0 < myn; j0 += 4 * 32) {
+        float tq[4], qv[4];
+        int pos[4];
+        bool k[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + u * 32;
+          k[u] = false;
+          pos[u] = 0;
+          tq[u] = 0.0f;
+          if (j < myn && listed_survivor(j)) {
+            const raw r = (raw)seg[j];
+            pos[u] = (int)segi[j];
+            see_last(r, pos[u]);
+            tq[u] = t_of(r);
+            k[u] = tq[u] >= lmp;
+            if (k[u] && orow) orow[pos[u]] = r;
+          }
+          qv[u] = (k[u] && race_on) ? __ldg(qr + pos[u]) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (k[u] && race_on) race(tq[u], qv[u], pos[u]);
       }
     } else {
+      if (tid == 0) h.rcount = 0;
+      __syncthreads();
       sweep(Loads<kLoadsSimple>{}, ReadAs<kReadLast>{}, [&](int e, const uint4& qin, int nv) {
         const uint32_t sb = survivor_bits(qin, nv);
-        if (nv == 0) return;
         uint32_t kb = 0;
+        float tv[VEC];
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
+          tv[j] = 0.0f;
           if ((sb >> j) & 1u) {
             const raw r = vec_elem<DT>(qin, j);
             see_last(r, e + j);
-            if (keep_race(r, e + j)) kb |= 1u << j;
+            tv[j] = t_of(r);
+            if (tv[j] >= lmp) kb |= 1u << j;
           }
         }
-        if (orow) write_vec(e, qin, nv, kb);
+        if (race_on) {
+          // list the kept elements: one warp scan, one shared atomic per warp
+          const uint32_t n = __popc(kb);
+          if (__any_sync(0xffffffffu, n != 0)) {
+            const uint32_t incl = warp_incl_scan(n);
+            uint32_t base = 0;
+            if (lane == 31) base = atomicAdd(&h.rcount, incl);
+            base = __shfl_sync(0xffffffffu, base, 31) + incl - n;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+              if ((kb >> j) & 1u) {
+                if (base < (uint32_t)kRaceCap) {
+                  rpos[base] = (uint32_t)(e + j);
+                  rt[base] = tv[j];
+                }
+                ++base;
+              }
+            }
+          }
+        }
+        if (nv != 0 && orow) write_vec(e, qin, nv, kb);
       });
+      if (race_on) {
+        __syncthreads();
+        const uint32_t nl = h.rcount;
+        if (nl <= (uint32_t)kRaceCap) {
+          for (uint32_t t0 = tid; t0 < nl; t0 += 4 * kThreads) {
+            float tq[4], qv[4];
+            int pos[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t j = t0 + u * kThreads;
+              pos[u] = j < nl ? (int)rpos[j] : -1;
+              tq[u] = j < nl ? rt[j] : 0.0f;
+              qv[u] = j < nl ? __ldg(qr + pos[u]) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (pos[u] >= 0) race(tq[u], qv[u], pos[u]);
+          }
+        } else {
+          // more candidates than the list holds: race them in a second sweep
+          seen = seen0;
+          sweep(Loads<kLoadsSimple>{}, ReadAs<kReadCg>{}, [&](int e, const uint4& qin, int nv) {
+            const uint32_t sb = survivor_bits(qin, nv);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+              if ((sb >> j) & 1u) {
+                const float tj = t_of(vec_elem<DT>(qin, j));
+                if (tj >= lmp) race(tj, __ldg(qr + e + j), e + j);
+              }
+            }
+          });
+        }
+      }
     }
     if (a.token) {
       unsigned long long pick;

@@ -207,9 +207,20 @@ __global__ void __launch_bounds__(kThreads, 1) v2_topk_kernel(const V2Args a) {
     const int sh = KB - 8 * (pass + 1);
     for (int i = tid; i < kWarps * 256; i += kThreads) (&s.whist[0][0])[i] = 0;
     __syncthreads();
-    for (int i = wb + lane; i < we; i += 32) {
-      const uint32_t key = order_key<DT>(xr[i]);
-      if (pass == 0 || (key >> (sh + 8)) == prefix) atomicAdd(&s.whist[warp][(key >> sh) & 255u], 1u);
+    for (int i0 = wb; i0 < we; i0 += 32 * 8) {
+      raw r[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * 32 + lane;
+        r[u] = i < we ? xr[i] : (raw)0;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (i0 + u * 32 + lane < we) {
+          const uint32_t key = order_key<DT>(r[u]);
+          if (pass == 0 || (key >> (sh + 8)) == prefix) atomicAdd(&s.whist[warp][(key >> sh) & 255u], 1u);
+        }
+      }
     }
     __syncthreads();
     if (tid < 256) {

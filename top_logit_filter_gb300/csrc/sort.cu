@@ -5,18 +5,20 @@
 // original index) and sorted_indices (int32 original positions).
 //
 // A least-significant-digit radix sort per row on the order keys of
-// common.cuh (-0 and +0 share a key, so they stay in index order), one
-// 8-bit digit per pass: 2 passes for 16-bit keys, 4 for fp32.  Passes
-// alternate between the caller's workspace and the outputs so that the last
-// one writes the outputs.  Every pass:
-//   1. counts the row's digits (256 bins) and scans them into bucket bases;
-//   2. walks the row in index order, 512 elements per tile (one per
-//      thread); a warp finds the lanes holding the same digit with eight
-//      ballots, the warps' per-digit counts are scanned in warp order, and
-//      a running count per digit carries the earlier tiles, so every element
-//      lands at base + earlier tiles + earlier warps + earlier lanes: a
-//      stable counting sort on the digit.
-// One 512-thread CTA per row; only shared-memory barriers, no waits.
+// common.cuh (-0 and +0 share a key, so they stay in index order), 8-bit
+// digits: 2 passes for 16-bit keys, 4 for fp32.  One 512-thread CTA per
+// row.  The row is read once to count every pass's digits (P histograms of
+// 256 bins, scanned into bucket bases).  Then every pass walks its source in
+// index order, 4096 elements per tile (eight per thread; warp w holds
+// elements w*256 .. w*256+255 of the tile, lanes consecutive): a warp ranks
+// each element among the earlier equal digits of its warp (one match_any finds
+// the lanes with its digit) and a per-warp running count per digit; the warps'
+// counts are scanned in warp order per digit, and a running count per digit
+// carries the earlier tiles, so every element lands at base + earlier tiles
+// + earlier warps + its rank in the warp: a stable counting sort on the
+// digit.  Passes alternate between the caller's workspace and the outputs
+// so that the last one writes the outputs.  Only CTA barriers, no waits;
+// every scatter position is checked against V.
 #include <cstdio>
 #include <mutex>
 
@@ -28,6 +30,21 @@ namespace topkp {
 namespace {
 
 constexpr int kDigits = 256;
+constexpr int kPer = 8;                        // elements per thread per tile
+constexpr int kTile = kThreads * kPer;         // 4096
+constexpr int kWarpSpan = 32 * kPer;           // 256 consecutive elements per warp per tile
+
+struct SortShared {
+  uint32_t base[4][kDigits];                   // bucket bases of every pass
+  uint32_t running[kDigits];                   // elements of earlier tiles per digit
+  uint32_t lstart[kDigits];                    // where a digit's elements start in the staged tile
+  uint32_t gstart[kDigits];                    // where they go in the destination
+  uint32_t wcnt[kWarps][kDigits];              // this tile's count per warp and digit
+  uint32_t woff[kWarps][kDigits];              // where a warp's elements of a digit start in the stage
+  uint32_t tmp[kWarps];
+  uint32_t stage_v[kTile];                     // the tile ordered by digit (raw bits)
+  int32_t stage_i[kTile];                      // and the elements' original indices
+};
 
 // Exclusive scan of v over the first 256 threads (every thread calls it);
 // returns the scan in threads 0..255.
@@ -51,16 +68,12 @@ __device__ __forceinline__ uint32_t scan256(uint32_t v, uint32_t* tmp) {
 }  // namespace
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 1) sort_kernel(const SortArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) sort_kernel(const SortArgs a) {
   using D = DType<DT>;
   using raw = typename D::raw;
   constexpr int P = D::kKeyBits / 8;  // digit passes
-  __shared__ uint32_t hist[kDigits];
-  __shared__ uint32_t base[kDigits];
-  __shared__ uint32_t running[kDigits];
-  __shared__ uint32_t wcount[kWarps][kDigits];
-  __shared__ uint32_t woff[kWarps][kDigits];
-  __shared__ uint32_t tmp[kWarps];
+  extern __shared__ __align__(16) unsigned char sort_smem[];
+  SortShared& s = *reinterpret_cast<SortShared*>(sort_smem);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.x;
@@ -78,8 +91,36 @@ __global__ void __launch_bounds__(kThreads, 1) sort_kernel(const SortArgs a) {
   raw* ws_v = reinterpret_cast<raw*>(a.ws_value) + row * (int64_t)V;
   int32_t* ws_i = a.ws_index + row * (int64_t)V;
   const uint32_t lt_mask = (1u << lane) - 1u;
+  auto key_of = [&](raw r) -> uint32_t { return order_key<DT>(r) ^ kinv; };
 
-  for (int i = tid; i < kWarps * kDigits; i += kThreads) (&wcount[0][0])[i] = 0;
+  // ---- every pass's digit counts from one read, scanned into bucket bases ----
+  for (int i = tid; i < 4 * kDigits; i += kThreads) (&s.base[0][0])[i] = 0;
+  for (int i = tid; i < kWarps * kDigits; i += kThreads) (&s.wcnt[0][0])[i] = 0;
+  __syncthreads();
+  for (int i0 = 0; i0 < V; i0 += kTile) {
+    raw r[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = i0 + u * kThreads + tid;
+      r[u] = i < V ? xr[i] : (raw)0;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      if (i0 + u * kThreads + tid < V) {
+        const uint32_t key = key_of(r[u]);
+#pragma unroll
+        for (int p = 0; p < P; ++p) atomicAdd(&s.base[p][(key >> (8 * p)) & 255u], 1u);
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    const uint32_t hv = tid < kDigits ? s.base[p][tid] : 0u;
+    const uint32_t ex = scan256(hv, s.tmp);
+    if (tid < kDigits) s.base[p][tid] = ex;
+  }
+  __syncthreads();
 
   for (int pass = 0; pass < P; ++pass) {
     const int shift = 8 * pass;
@@ -89,62 +130,82 @@ __global__ void __launch_bounds__(kThreads, 1) sort_kernel(const SortArgs a) {
     int32_t* di = to_out ? out_i : ws_i;
     const raw* sv = pass == 0 ? xr : (to_out ? ws_v : out_v);
     const int32_t* si = to_out ? ws_i : out_i;  // unused in pass 0
-    auto digit_of = [&](raw r) -> uint32_t { return ((order_key<DT>(r) ^ kinv) >> shift) & 255u; };
-
-    // ---- 1. digit counts and bucket bases ----
-    if (tid < kDigits) hist[tid] = 0;
-    __syncthreads();
-    for (int i = tid; i < V; i += kThreads) atomicAdd(&hist[digit_of(sv[i])], 1u);
-    __syncthreads();
-    const uint32_t hv = tid < kDigits ? hist[tid] : 0u;
-    const uint32_t ex = scan256(hv, tmp);
-    if (tid < kDigits) {
-      base[tid] = ex;
-      running[tid] = 0;
-    }
+    if (tid < kDigits) s.running[tid] = 0;
     __syncthreads();
 
-    // ---- 2. stable scatter, one element per thread per tile ----
-    for (int t0 = 0; t0 < V; t0 += kThreads) {
-      const int i = t0 + tid;
-      const bool valid = i < V;
-      raw r = 0;
-      int32_t ix = 0;
-      uint32_t d = 0;
-      if (valid) {
-        r = sv[i];
-        ix = pass == 0 ? i : si[i];
-        d = digit_of(r);
-      }
-      // lanes holding the same digit
-      uint32_t peers = __ballot_sync(0xffffffffu, valid);
+    for (int t0 = 0; t0 < V; t0 += kTile) {
+      raw r[kPer];
+      int32_t ix[kPer];
+      uint32_t d[kPer], rk[kPer];
+      const int wbase = t0 + warp * kWarpSpan;
+      // every load of the tile in flight before any is used
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const uint32_t m = __ballot_sync(0xffffffffu, (d >> b) & 1u);
-        peers &= ((d >> b) & 1u) ? m : ~m;
+      for (int u = 0; u < kPer; ++u) {
+        const int i = wbase + u * 32 + lane;
+        r[u] = 0;
+        ix[u] = 0;
+        if (i < V) {
+          r[u] = sv[i];
+          ix[u] = pass == 0 ? i : si[i];
+        }
       }
-      const uint32_t lower = __popc(peers & lt_mask);
-      if (valid && lower == 0) wcount[warp][d] = __popc(peers);
+      // ---- rank every element among the earlier equal digits of its warp ----
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const bool valid = wbase + u * 32 + lane < V;
+        d[u] = valid ? (key_of(r[u]) >> shift) & 255u : 256u;  // 256: invalid lanes match only each other
+        const uint32_t peers = __match_any_sync(0xffffffffu, d[u]);  // the lanes holding the same digit
+        const uint32_t before = valid ? s.wcnt[warp][d[u]] : 0u;
+        rk[u] = before + __popc(peers & lt_mask);
+        __syncwarp();
+        if (valid && (peers & lt_mask) == 0) s.wcnt[warp][d[u]] = before + __popc(peers);
+        __syncwarp();
+      }
       __syncthreads();
+      // ---- the tile's count per digit, scanned: where each digit's run
+      // starts in the staged tile and in the destination ----
+      uint32_t tc = 0;
       if (tid < kDigits) {
-        uint32_t acc = running[tid];
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) tc += s.wcnt[w][tid];
+      }
+      const uint32_t ls = scan256(tc, s.tmp);
+      if (tid < kDigits) {
+        uint32_t acc = ls;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-          const uint32_t c = wcount[w][tid];
-          woff[w][tid] = acc;
+          const uint32_t c = s.wcnt[w][tid];
+          s.woff[w][tid] = acc;
           acc += c;
-          wcount[w][tid] = 0;
+          s.wcnt[w][tid] = 0;
         }
-        running[tid] = acc;
+        s.lstart[tid] = ls;
+        s.gstart[tid] = s.base[pass][tid] + s.running[tid];
+        s.running[tid] += tc;
       }
       __syncthreads();
-      if (valid) {
-        const uint32_t pos = base[d] + woff[warp][d] + lower;
-        if (pos < (uint32_t)V) {
-          dv[pos] = r;
-          di[pos] = ix;
+      // ---- the tile staged in shared memory in digit order (stable) ----
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        if (d[u] < 256u) {
+          const uint32_t L = s.woff[warp][d[u]] + rk[u];
+          s.stage_v[L] = (uint32_t)r[u];
+          s.stage_i[L] = ix[u];
         }
       }
+      __syncthreads();
+      // ---- each digit's run written to consecutive destination positions ----
+      const int tn = min(kTile, V - t0);
+      for (int L = tid; L < tn; L += kThreads) {
+        const raw rv = (raw)s.stage_v[L];
+        const uint32_t dd = (key_of(rv) >> shift) & 255u;
+        const uint32_t pos = s.gstart[dd] + ((uint32_t)L - s.lstart[dd]);
+        if (pos < (uint32_t)V) {
+          dv[pos] = rv;
+          di[pos] = s.stage_i[L];
+        }
+      }
+      __syncthreads();  // the stage is free for the next tile
     }
     __syncthreads();  // this pass's writes before the next pass reads them
   }
@@ -152,7 +213,16 @@ __global__ void __launch_bounds__(kThreads, 1) sort_kernel(const SortArgs a) {
 
 template <int DT>
 static cudaError_t launch_sort_dt(const SortArgs& a, cudaStream_t s) {
-  sort_kernel<DT><<<dim3((unsigned)a.B), dim3(kThreads), 0, s>>>(a);
+  static thread_local int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(sort_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SortShared));
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  sort_kernel<DT><<<dim3((unsigned)a.B), dim3(kThreads), sizeof(SortShared), s>>>(a);
   return cudaGetLastError();
 }
 
