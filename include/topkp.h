@@ -107,6 +107,10 @@ typedef int topkp_status;
  *              out == logits with ld_out == ld_logits (in place) is allowed;
  *              any other overlap with logits, p or k is rejected.
  *   stream     cudaStream_t to launch on.
+ * Rows of at most 4096 elements, and 16-bit rows of at most 32768, run on a
+ * kernel that holds each row on chip (one block per row); longer rows on the
+ * main filter kernel.  Both give the same bits.  One kernel launch per
+ * 2^31 - 1 blocks.
  */
 topkp_status topkp_apply(const void* logits, int64_t B, int64_t V, int64_t ld_logits,
                          topkp_dtype dtype, const void* p, const int32_t* k,

@@ -207,7 +207,11 @@ topkp_status apply_impl(const char* fn, const void* logits, int64_t B, int64_t V
   a.ldx = ld_logits;
   a.ldo = out ? ld_out : V;
   a.V = (int32_t)V;
-  const ApplyPlan plan = plan_apply(B, V, k != nullptr, sms, getenv("TOPKP_FORCE_PLAN"));
+  // Short rows take the on-chip kernels (small.cu) unless a plan of the main
+  // kernel is forced; "small" forces them wherever the shape allows.
+  const char* force = getenv("TOPKP_FORCE_PLAN");
+  const bool small = !fused && small_rows(dtype, V) && (!force || !*force || strcmp(force, "small") == 0);
+  const ApplyPlan plan = small ? ApplyPlan{} : plan_apply(B, V, k != nullptr, sms, force);
   a.cs = plan.cs;
   a.mixed = plan.mixed;
   a.force = plan.force_bits;
@@ -231,11 +235,12 @@ topkp_status apply_impl(const char* fn, const void* logits, int64_t B, int64_t V
     ai.min_p = min_p ? min_p + r0 : nullptr;
     ai.q = q ? q + r0 * ldq : nullptr;
     ai.token = token ? token + r0 : nullptr;
-    const cudaError_t e = launch_apply(dtype, ai, (cudaStream_t)stream);
+    const cudaError_t e = small ? launch_apply_small(dtype, ai, (cudaStream_t)stream)
+                                : launch_apply(dtype, ai, (cudaStream_t)stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
-      return fail(TOPKP_ERR_LAUNCH, "%s: launch failed (%s; cs=%d smem=%zu)", fn, cudaGetErrorString(e), a.cs,
-                  kApplySmem);
+      return fail(TOPKP_ERR_LAUNCH, "%s: launch failed (%s; %s, cs=%d)", fn, cudaGetErrorString(e),
+                  small ? "short-row kernel" : "main kernel", a.cs);
     }
     ++launches;
   }

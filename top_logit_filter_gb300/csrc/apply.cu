@@ -41,9 +41,10 @@
 //      window of buckets; each window bucket gets 16 per-key counters (only
 //      the occupied ones when a window crossing zero spans too many);
 //   3. pass B computes every element's mass: the row total and the mass
-//      below the window accumulate in registers (fp32 per 16-byte vector,
-//      then 2^-40 fixed point), the few elements inside the window are
-//      counted per key; the cut follows from count x mass per key.
+//      below the window accumulate in registers (each element's 2^-40
+//      fixed-point mass, so every path sums the same integers), the few
+//      elements inside the window are counted per key; the cut follows from
+//      count x mass per key.
 // Everything else (fp32 top-p-only rows, overflowing lists, windows with too
 // many occupied buckets) takes the generic path: a radix descent over the
 // whole row (11-bit first digit, then 5 bits for 16-bit keys or 11 + 10 for
@@ -1219,40 +1220,27 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
       __syncthreads();
       const uint32_t wkey0 = (uint32_t)w0 << SHB;
       const uint32_t nwin = (uint32_t)nocc * 16u;  // counters in use
-      // pass B (from L2): row mass and mass below the window (fp32 per
-      // vector, then fixed point), per-key counts inside the window.  Window
-      // membership is a float compare: key order is value order.
+      // pass B (from L2): row mass and mass below the window (every
+      // element's fixed-point mass, so the sums equal those of the other
+      // paths exactly), per-key counts inside the window.  Window membership
+      // is a float compare: key order is value order.
       const float lo_f = value_of_key<DT>((uint32_t)w0 << SHB);
-      const float hi_f = value_of_key<DT>(((uint32_t)w1 << SHB) | ((1u << SHB) - 1u));
       unsigned long long s_mine = 0, b_mine = 0;
-      float s_run = 0.0f, b_run = 0.0f;  // fp32 over up to kRun vectors, then fixed point
-      int n_run = 0;
-      constexpr int kRun = 4;
       const uint32_t LO2 = P::splat((uint32_t)raw_of_key<DT>((uint32_t)w0 << SHB));
       const uint32_t HI2 = P::splat((uint32_t)raw_of_key<DT>(((uint32_t)w1 << SHB) | ((1u << SHB) - 1u)));
       sweep(Loads<kLoadsHeavy>{}, ReadAs<kReadCg>{}, [&](int, const uint4& q, int nv) {
-        // two values per word: one packed fma, two exponentials, one packed
-        // add; the -inf padding has zero mass, so no element mask is needed
-        float2 sv = make_float2(0.0f, 0.0f);
-        float bv = 0.0f;
+        // two values per word: one packed fma and two exponentials; the -inf
+        // padding has zero mass, so no element mask is needed
         const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
         uint32_t wm[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float2 x = P::unpack2(wd[i]);
           const float2 e = mass2_f32(x, mr);
-          sv = add2_f32(sv, e);
-          if (x.x < lo_f) bv += e.x;
-          if (x.y < lo_f) bv += e.y;
+          const unsigned long long m0 = f2ull_rn(e.x * kMassScaleF), m1 = f2ull_rn(e.y * kMassScaleF);
+          s_mine += m0 + m1;
+          b_mine += (x.x < lo_f ? m0 : 0ull) + (x.y < lo_f ? m1 : 0ull);
           wm[i] = P::ge(wd[i], LO2) & ~P::gt(wd[i], HI2);
-        }
-        s_run += sv.x + sv.y;
-        b_run += bv;
-        if (++n_run == kRun) {
-          s_mine += f2ull_rn(s_run * kMassScaleF);
-          b_mine += f2ull_rn(b_run * kMassScaleF);
-          s_run = b_run = 0.0f;
-          n_run = 0;
         }
         // the few elements inside the window: independent, predicated counts
         const uint32_t inwin = mask_bits<KB>(wm[0], wm[1], wm[2], wm[3]) & ((1u << nv) - 1u);
@@ -1268,8 +1256,6 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
           }
         }
       });
-      s_mine += f2ull_rn(s_run * kMassScaleF);
-      b_mine += f2ull_rn(b_run * kMassScaleF);
       unsigned long long d0, d1, sb[2];
       block_exclusive_scan2(s_mine, b_mine, &d0, &d1, &sb[0], &sb[1], h.ws);
       cl_reduce<kClSum, 2>(cl, h.cx, cph, sb);  // (its barrier also completes every CTA's window counters)

@@ -132,7 +132,8 @@ __host__ __device__ __forceinline__ uint32_t float_bits(float f) {
 __host__ __device__ __forceinline__ unsigned long long f2ull_rn(float f) {
   // Below 2^23, adding 2^23 leaves the integer part in the mantissa, rounded
   // to nearest with ties to even by the fp32 add itself.  From 2^23 on, a
-  // float is an integer: its mantissa shifted by the exponent.
+  // float is an integer: its mantissa shifted by the exponent.  (The
+  // conversion instruction to 64 bits runs on the narrow FP64 pipe.)
   if (f < 8388608.0f) return (unsigned long long)(float_bits(f + 8388608.0f) - 0x4b000000u);
   const uint32_t b = float_bits(f);
   return (unsigned long long)((b & 0x7fffffu) | 0x800000u) << ((b >> 23) - 150u);

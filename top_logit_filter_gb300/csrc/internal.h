@@ -71,6 +71,22 @@ ApplyPlan plan_apply(int64_t B, int64_t V, bool has_k, int num_sms, const char* 
 
 cudaError_t launch_apply(topkp_dtype dt, const ApplyArgs& a, cudaStream_t s);
 
+// Short rows (small.cu): one CTA per row holds the whole row on chip.  Rows
+// of at most kSmallSortMaxV elements (any dtype) are sorted in shared memory;
+// 16-bit rows of at most kSmallTableMaxV elements stay in registers and are
+// counted per key.  Same results as launch_apply, bit for bit; no cluster,
+// no fused sample.
+constexpr int kSmallSortMaxV = 4096;
+constexpr int kSmallTableMaxV = 32768;
+constexpr size_t kSmallHdrBytes = 512;
+constexpr size_t kSmallSortSmem = kSmallHdrBytes + (size_t)kSmallSortMaxV * (8 + 4 + 1);
+constexpr size_t kSmallTableSmem = kSmallHdrBytes + 65536 * 2 + 4096 * (4 + 8);
+// Whether a row shape takes the short-row kernels.
+inline bool small_rows(topkp_dtype dt, int64_t V) {
+  return V <= kSmallSortMaxV || (dt != TOPKP_F32 && V <= kSmallTableMaxV);
+}
+cudaError_t launch_apply_small(topkp_dtype dt, const ApplyArgs& a, cudaStream_t s);
+
 // --------------------------------------------------------------- sorted
 struct SortedArgs {
   const void* sv;          // sorted_value [B, V]

@@ -1,0 +1,570 @@
+// topkp_apply for short rows: one CTA holds the whole row on chip, so the row
+// is read once and every step after the load runs in registers and shared
+// memory, with a handful of block-wide steps and compact code.
+//
+// What it computes is the eight-step formula of [guide] §2, exactly as the
+// main filter kernel (apply.cu) computes it: the same order keys, the same
+// per-element masses in 2^-40 fixed point relative to the row maximum, the
+// same integer sums, so both reach the same cut in the stable order and
+// write the same bits.
+//
+// Two kernels:
+//   * rows of at most 4096 elements (any dtype): the row is sorted in shared
+//     memory by (order key, position), a bitonic sort, which is the stable
+//     ascending sort of [guide] §2 step 1; the k-th largest is read off the
+//     sorted row, the masses of the survivors are scanned in sorted order,
+//     and position j is kept when its cumulative mass exceeds
+//     floor(round_D(1 - p) x total) or it is the last position;
+//   * 16-bit rows of at most 32768 elements: every thread keeps eight
+//     16-byte vectors of the row in registers, and one table of per-key
+//     counts (two 16-bit counters per word, 128 KB) gives every key's exact
+//     mass as count x mass(key).  The top-k threshold and the top-p cut follow
+//     from two block scans over the table in descending key order; ties of
+//     the cut are ranked by position from per-vector tie counts.
+#include "common.cuh"
+#include "internal.h"
+
+namespace topkp {
+
+namespace {
+
+constexpr int kVecPerThread = kSmallTableMaxV / kThreads / 8;  // 16-byte vectors of 16-bit elements per thread
+static_assert(kVecPerThread == 8, "table kernel layout");
+constexpr int kTabWords = 65536 / 2;                            // two 16-bit key counters per word
+
+struct SmallHdr {
+  unsigned long long ws[2 * kWarps];  // block-scan scratch
+  unsigned long long part;            // table kernel: survivors' mass in the block holding the top-k threshold
+  uint32_t maxkey;
+  uint32_t kkey;                      // top-k threshold key (0: none)
+  uint32_t tkey;                      // cut key
+  uint32_t r0;                        // ties of the cut key masked, in index order
+  uint32_t kblock;                    // table kernel: block holding the top-k threshold
+  uint32_t wblk;                      // table kernel: block holding the top-p cut
+  unsigned long long wabove;          // table kernel: count or mass above the walked block
+};
+
+// ------------------------------------------------------------ sort kernel
+// Shared memory: the header, n (key << 32 | position) entries, the row's raw
+// values and one keep flag per element.
+constexpr size_t kSortEntOff = kSmallHdrBytes;
+constexpr size_t kSortRowOff = kSortEntOff + (size_t)kSmallSortMaxV * 8;
+constexpr size_t kSortFlagOff = kSortRowOff + (size_t)kSmallSortMaxV * 4;
+static_assert(8 * kThreads == kSmallSortMaxV, "every position has a thread at eight per thread");
+static_assert(sizeof(SmallHdr) <= kSmallHdrBytes, "header fits");
+
+// One bitonic stage of stride S < E on the E positions a thread holds
+// (positions tid*E + r).
+template <int S, int E>
+__device__ __forceinline__ void sort_stage_in_thread(unsigned long long (&v)[E], int tid, int size) {
+#pragma unroll
+  for (int r = 0; r < E; ++r) {
+    if ((r & S) == 0) {
+      const bool asc = ((tid * E + r) & size) == 0;
+      const unsigned long long x = v[r], y = v[r + S];
+      const bool swap = (x > y) == asc;
+      v[r] = swap ? y : x;
+      v[r + S] = swap ? x : y;
+    }
+  }
+}
+
+template <int DT, int E>
+__global__ void __launch_bounds__(kThreads, 1) small_sort_kernel(const ApplyArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  using D = DType<DT>;
+  using raw = typename D::raw;
+  SmallHdr& h = *reinterpret_cast<SmallHdr*>(smem);
+  unsigned long long* ent = reinterpret_cast<unsigned long long*>(smem + kSortEntOff);
+  raw* rowv = reinterpret_cast<raw*>(smem + kSortRowOff);
+  uint8_t* keepf = smem + kSortFlagOff;
+
+  const int tid = threadIdx.x;
+  const int64_t row = blockIdx.x;
+  const int V = a.V;
+  const raw* xr = reinterpret_cast<const raw*>(a.x) + row * a.ldx;
+  raw* orow = reinterpret_cast<raw*>(a.out) + row * a.ldo;
+  const int kv = a.k ? a.k[row] : 0;
+  const bool topk = a.k != nullptr && kv >= 1 && kv <= V - 1;
+  const bool topp = a.p != nullptr;
+  if (!topk && !topp) {  // nothing to filter: a copy, or nothing in place
+    if (reinterpret_cast<const void*>(xr) != reinterpret_cast<const void*>(orow))
+      for (int i = tid; i < V; i += kThreads) orow[i] = xr[i];
+    return;
+  }
+  const float thr = topp ? top_p_threshold<DT>(a.p, row) : 0.0f;
+
+  int n = 1;
+  while (n < V) n <<= 1;
+  // thread t holds positions E t .. E t + E - 1 of the n entries, E = n / 512
+  // (at least 1; threads past n / E hold padding only, and their warps skip
+  // the compare stages)
+  const bool live = (tid >> 5) * 32 * E < n;  // warp-uniform
+  unsigned long long v[E];
+#pragma unroll
+  for (int r = 0; r < E; ++r) {
+    const int i = tid * E + r;
+    v[r] = ~0ull;  // above every element: the padding sorts last
+    if (i < V) {
+      const raw x = xr[i];
+      rowv[i] = x;
+      v[r] = ((unsigned long long)order_key<DT>(x) << 32) | (unsigned long long)i;
+    }
+  }
+  // bitonic sort, ascending: (key, position) is the stable order.  A stage
+  // of stride s compares position i with i ^ s, ascending where i & size is
+  // 0: within a thread for s < E, between the lanes of a warp for s < 32 E,
+  // through shared memory beyond.
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= 32 * E) {
+#pragma unroll
+        for (int r = 0; r < E; ++r) ent[tid * E + r] = v[r];
+        __syncthreads();
+        if (live) {
+#pragma unroll
+          for (int r = 0; r < E; ++r) {
+            const int i = tid * E + r;
+            const unsigned long long y = ent[i ^ stride];
+            const bool keep_min = ((i & size) == 0) == ((i & stride) == 0);
+            v[r] = keep_min ? min(v[r], y) : max(v[r], y);
+          }
+        }
+        __syncthreads();
+      } else if (live) {
+        if (stride >= E) {
+          const int lm = stride / E;  // partner lane distance
+#pragma unroll
+          for (int r = 0; r < E; ++r) {
+            const int i = tid * E + r;
+            const unsigned long long y = __shfl_xor_sync(0xffffffffu, v[r], lm);
+            const bool keep_min = ((i & size) == 0) == ((i & stride) == 0);
+            v[r] = keep_min ? min(v[r], y) : max(v[r], y);
+          }
+        } else {
+          if constexpr (E >= 8) {
+            if (stride == 4) sort_stage_in_thread<4, E>(v, tid, size);
+          }
+          if constexpr (E >= 4) {
+            if (stride == 2) sort_stage_in_thread<2, E>(v, tid, size);
+          }
+          if constexpr (E >= 2) {
+            if (stride == 1) sort_stage_in_thread<1, E>(v, tid, size);
+          }
+        }
+      }
+    }
+  }
+  if (tid == 0) {
+    h.maxkey = 0;
+    h.kkey = 0;
+  }
+  __syncthreads();
+  // the max (position V-1) and the k-th largest (position V-k; ties of it survive)
+#pragma unroll
+  for (int r = 0; r < E; ++r) {
+    const int j = tid * E + r;
+    if (j == V - 1) h.maxkey = (uint32_t)(v[r] >> 32);
+    if (topk && j == V - kv) h.kkey = (uint32_t)(v[r] >> 32);
+  }
+  __syncthreads();
+  const uint32_t maxkey = h.maxkey;
+  const uint32_t kkey = h.kkey;
+  const MassRef mr(value_of_key<DT>(maxkey));
+  unsigned long long m[E];
+  unsigned long long mine = 0;
+#pragma unroll
+  for (int r = 0; r < E; ++r) {
+    m[r] = 0;
+    const int j = tid * E + r;
+    if (topp && j < V) {
+      const uint32_t key = (uint32_t)(v[r] >> 32);
+      if (key >= kkey) m[r] = mass_fixed(value_of_key<DT>(key), mr);
+      mine += m[r];
+    }
+  }
+  unsigned long long S = 0, acc = 0;
+  if (topp) acc = block_exclusive_scan(mine, &S, h.ws);
+  const unsigned long long target = mass_target(thr, S);
+#pragma unroll
+  for (int r = 0; r < E; ++r) {
+    const int j = tid * E + r;
+    if (j < V) {
+      const uint32_t key = (uint32_t)(v[r] >> 32);
+      acc += m[r];
+      // masked when the cumulative mass is <= the threshold, except the last position
+      const bool keep = key >= kkey && (!topp || acc > target || j == V - 1);
+      keepf[(uint32_t)v[r]] = keep ? 1 : 0;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < V; i += kThreads) orow[i] = keepf[i] ? rowv[i] : D::kNegInf;
+}
+
+// ----------------------------------------------------------- table kernel
+constexpr size_t kTabOff = kSmallHdrBytes;
+constexpr int kTabBuckets = 65536 / 16;                                      // 16-key buckets
+constexpr size_t kBcntOff = kTabOff + (size_t)kTabWords * 4;                 // [kTabBuckets] counts
+constexpr size_t kBmassOff = kBcntOff + (size_t)kTabBuckets * 4;             // [kTabBuckets] masses
+
+template <int DT>
+__device__ __forceinline__ uint32_t half_key(uint32_t w, int j) {
+  return order_key<DT>((uint16_t)(j ? (w >> 16) : (w & 0xffffu)));
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  using D = DType<DT>;
+  using raw = typename D::raw;
+  static_assert(D::kKeyBits == 16, "16-bit keys");
+  SmallHdr& h = *reinterpret_cast<SmallHdr*>(smem);
+  uint32_t* tab = reinterpret_cast<uint32_t*>(smem + kTabOff);
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x;
+  const int V = a.V;
+  const raw* xr = reinterpret_cast<const raw*>(a.x) + row * a.ldx;
+  raw* orow = reinterpret_cast<raw*>(a.out) + row * a.ldo;
+  const int kv = a.k ? a.k[row] : 0;
+  const bool topk = a.k != nullptr && kv >= 1 && kv <= V - 1;
+  const bool topp = a.p != nullptr;
+  const bool in_place = reinterpret_cast<const void*>(xr) == reinterpret_cast<const void*>(orow);
+  if (!topk && !topp) {
+    if (!in_place)
+      for (int i = tid; i < V; i += kThreads) orow[i] = xr[i];
+    return;
+  }
+  const float thr = topp ? top_p_threshold<DT>(a.p, row) : 0.0f;
+  const bool xvec = (reinterpret_cast<uintptr_t>(xr) & 15u) == 0;
+  const bool ovec = (reinterpret_cast<uintptr_t>(orow) & 15u) == 0;
+  const uint32_t NEG2 = (uint32_t)D::kNegInf * 0x10001u;
+
+  // ---- load: vector v = u * kThreads + tid holds elements 8v .. 8v+7 ----
+  uint4 q[kVecPerThread];
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    const int e = (u * kThreads + tid) * 8;
+    q[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
+    if (e + 8 <= V && xvec) {
+      asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(q[u].x), "=r"(q[u].y), "=r"(q[u].z), "=r"(q[u].w)
+                   : "l"(xr + e));
+    } else if (e < V) {
+      uint32_t w[4] = {NEG2, NEG2, NEG2, NEG2};
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (e + j < V) {
+          const int sh = (j & 1) * 16;
+          w[j >> 1] = (w[j >> 1] & ~(0xffffu << sh)) | ((uint32_t)xr[e + j] << sh);
+        }
+      q[u] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  // the table is cleared while the loads are in flight
+  for (int i = tid; i < kTabWords / 4; i += kThreads) reinterpret_cast<uint4*>(tab)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    h.maxkey = 0;
+    h.kkey = 0;
+    h.kblock = 0;
+    h.wblk = 0;
+    h.wabove = 0;
+    h.part = 0;
+    h.tkey = 0;
+    h.r0 = 0;
+  }
+  __syncthreads();
+
+  // ---- per-key counts and the row max ----
+  uint32_t kmax = 0;
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    const int e = (u * kThreads + tid) * 8;
+    const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (e + j < V) {
+        const uint32_t key = half_key<DT>(wd[j >> 1], j & 1);
+        kmax = max(kmax, key);
+        atomicAdd(&tab[key >> 1], (key & 1u) ? 0x10000u : 1u);
+      }
+    }
+  }
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) atomicMax(&h.maxkey, kmax);
+  __syncthreads();
+  const uint32_t maxkey = h.maxkey;
+  const MassRef mr(value_of_key<DT>(maxkey));
+
+  // ---- per 16-key bucket its count and (top-p) its mass; thread t takes
+  // buckets t, t + 512, ... so that the dense key ranges spread over all
+  // threads ----
+  uint32_t* bcnt = reinterpret_cast<uint32_t*>(smem + kBcntOff);
+  unsigned long long* bmass = reinterpret_cast<unsigned long long*>(smem + kBmassOff);
+#pragma unroll 2
+  for (int i = 0; i < kTabBuckets / kThreads; ++i) {
+    const int b = i * kThreads + tid;
+    const uint4 wa = reinterpret_cast<const uint4*>(tab)[2 * b];
+    const uint4 wb = reinterpret_cast<const uint4*>(tab)[2 * b + 1];
+    const uint32_t ww[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+    uint32_t c = 0;
+    unsigned long long m = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      if (ww[w]) {
+        const uint32_t c0 = ww[w] & 0xffffu, c1 = ww[w] >> 16;
+        c += c0 + c1;
+        if (topp) {
+          const uint32_t key0 = (uint32_t)b * 16u + 2u * (uint32_t)w;
+          if (c0) m += (unsigned long long)c0 * mass_fixed(value_of_key<DT>(key0), mr);
+          if (c1) m += (unsigned long long)c1 * mass_fixed(value_of_key<DT>(key0 + 1u), mr);
+        }
+      }
+    }
+    bcnt[b] = c;
+    bmass[b] = m;
+  }
+  __syncthreads();
+  // ---- the table in descending key order: thread t owns the 128 keys
+  // (8 buckets) of block 511 - t ----
+  const uint32_t blk = (uint32_t)(kThreads - 1 - tid);
+  uint32_t cnt = 0;
+  unsigned long long mass = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    cnt += bcnt[blk * 8 + j];
+    mass += bmass[blk * 8 + j];
+  }
+  auto count_of = [&](uint32_t key) -> uint32_t {
+    const uint32_t w = tab[key >> 1];
+    return (key & 1u) ? (w >> 16) : (w & 0xffffu);
+  };
+  // Warp 0 walks block b down from its largest key, starting `above` from
+  // the top: the first key at which above + the counts (or masses, keys >=
+  // lo only) so far reach `goal`.  Lane l takes keys b*128 + 127 - 4l - i.
+  // Every lane gets the key and the sum before it.
+  auto warp_walk = [&](uint32_t b, unsigned long long above, unsigned long long goal, bool by_mass, uint32_t lo,
+                       unsigned long long* before) -> uint32_t {
+    b &= (uint32_t)(kThreads - 1);  // a block of the table
+    unsigned long long v[4], s = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t key = b * 128u + 127u - 4u * (uint32_t)lane - (uint32_t)i;
+      const uint32_t c = key >= lo ? count_of(key) : 0u;
+      v[i] = by_mass ? (c ? (unsigned long long)c * mass_fixed(value_of_key<DT>(key), mr) : 0ull) : c;
+      s += v[i];
+    }
+    unsigned long long incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const bool here = above + incl - s < goal && goal <= above + incl;
+    const int f = __ffs(__ballot_sync(0xffffffffu, here)) - 1;
+    uint32_t key = 0;
+    unsigned long long acc = above + incl - s;
+    if (here) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (acc + v[i] >= goal) {
+          key = b * 128u + 127u - 4u * (uint32_t)lane - (uint32_t)i;
+          break;
+        }
+        acc += v[i];
+      }
+    }
+    *before = __shfl_sync(0xffffffffu, acc, f < 0 ? 0 : f);
+    return __shfl_sync(0xffffffffu, key, f < 0 ? 0 : f);
+  };
+
+  // ---- top-k: the k-th largest key, from the counts above each block ----
+  uint32_t kkey = 0;
+  if (topk) {
+    unsigned long long tot;
+    const unsigned long long above = block_exclusive_scan(cnt, &tot, h.ws);
+    if (above < (unsigned long long)kv && (unsigned long long)kv <= above + cnt) {
+      h.kblock = blk;
+      h.wabove = above;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t b = h.kblock;
+      unsigned long long before;
+      const uint32_t key = warp_walk(b, h.wabove, (unsigned long long)kv, false, 0u, &before);
+      unsigned long long part = 0;  // mass of the block's keys >= the threshold
+      if (topp) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t kk = b * 128u + 127u - 4u * (uint32_t)lane - (uint32_t)i;
+          const uint32_t c = kk >= key ? count_of(kk) : 0u;
+          if (c) part += (unsigned long long)c * mass_fixed(value_of_key<DT>(kk), mr);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      }
+      if (lane == 0) {
+        h.kkey = key;
+        h.part = part;
+      }
+    }
+    __syncthreads();
+    kkey = h.kkey;
+    // survivors only: blocks below the threshold's block carry no mass, and
+    // that block only its keys >= the threshold
+    if (blk < h.kblock) mass = 0;
+    else if (blk == h.kblock) mass = h.part;
+  }
+
+  // ---- top-p: the cut, walking down from the largest key; an element is
+  // kept while the mass strictly above it is < R = S - floor(thr x S) ----
+  uint32_t T = kkey, r0 = 0;
+  if (topp) {
+    unsigned long long S;
+    const unsigned long long above = block_exclusive_scan(mass, &S, h.ws);
+    const unsigned long long R = S - mass_target(thr, S);
+    if (R != 0 && above < R && R <= above + mass) {
+      h.wblk = blk;
+      h.wabove = above;
+    }
+    __syncthreads();
+    if (R == 0) {
+      // only the last sorted position survives: the last element equal to the max
+      T = maxkey;
+      r0 = count_of(maxkey) - 1u;
+    } else {
+      if (warp == 0) {
+        unsigned long long base;
+        const uint32_t key = warp_walk(h.wblk, h.wabove, R, true, kkey, &base);
+        if (lane == 0) {
+          const unsigned long long u = mass_fixed(value_of_key<DT>(key), mr);
+          // the (R - base) / u rounded up ties of largest positions stay
+          const uint32_t c = count_of(key);
+          const unsigned long long keep = u ? (R - base + u - 1) / u : (unsigned long long)c;
+          h.tkey = key;
+          h.r0 = c - (uint32_t)min(keep, (unsigned long long)c);
+        }
+      }
+      __syncthreads();
+      T = h.tkey;
+      r0 = h.r0;
+    }
+  }
+
+  // ---- ties of T ranked by position: index order is (u, thread, element) ----
+  uint32_t tie_before[kVecPerThread];
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) tie_before[u] = 0;
+  if (r0 > 0) {
+    uint32_t tc[kVecPerThread];
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u) {
+      const int e = (u * kThreads + tid) * 8;
+      const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+      tc[u] = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (e + j < V && half_key<DT>(wd[j >> 1], j & 1) == T) ++tc[u];
+    }
+    // four 16-bit lanes per word: at most 8 x kThreads ties per vector round
+    unsigned long long pa = 0, pb = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      pa |= (unsigned long long)tc[u] << (16 * u);
+      pb |= (unsigned long long)tc[u + 4] << (16 * u);
+    }
+    unsigned long long ea, eb, ta, tb;
+    block_exclusive_scan2(pa, pb, &ea, &eb, &ta, &tb, h.ws);
+    uint32_t rounds = 0;  // ties in the earlier vector rounds
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u) {
+      const unsigned long long ex = u < 4 ? ea : eb, tot = u < 4 ? ta : tb;
+      const int sh = 16 * (u & 3);
+      tie_before[u] = rounds + (uint32_t)((ex >> sh) & 0xffffu);
+      rounds += (uint32_t)((tot >> sh) & 0xffffu);
+    }
+  }
+
+  // ---- write: the element, or -inf, in original order ([guide] §2 step 8) ----
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    const int e = (u * kThreads + tid) * 8;
+    if (e >= V) continue;
+    const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+    uint32_t o[4];
+    uint32_t rank = tie_before[u];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t b = (j & 1) ? (wd[j >> 1] >> 16) : (wd[j >> 1] & 0xffffu);
+      const uint32_t key = order_key<DT>((uint16_t)b);
+      bool keep = key > T;
+      if (key == T) {
+        keep = rank >= r0;
+        ++rank;
+      }
+      const uint32_t ob = keep ? b : (uint32_t)D::kNegInf;
+      if (j & 1) o[j >> 1] |= ob << 16;
+      else o[j >> 1] = ob;
+    }
+    if (e + 8 <= V && ovec) {
+      *reinterpret_cast<uint4*>(orow + e) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (e + j < V) orow[e + j] = (raw)((j & 1) ? (o[j >> 1] >> 16) : (o[j >> 1] & 0xffffu));
+    }
+  }
+}
+
+template <typename K>
+cudaError_t launch_small(K kern, size_t smem, const ApplyArgs& a, cudaStream_t s, int* configured_dev) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (*configured_dev != dev) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    *configured_dev = dev;
+  }
+  kern<<<(unsigned)a.B, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_sort_path(const ApplyArgs& a, cudaStream_t s) {
+  // positions per thread: the padded row over 512 threads
+  static thread_local int dev[4] = {-1, -1, -1, -1};
+  if (a.V > 2048) return launch_small(small_sort_kernel<DT, 8>, kSmallSortSmem, a, s, &dev[3]);
+  if (a.V > 1024) return launch_small(small_sort_kernel<DT, 4>, kSmallSortSmem, a, s, &dev[2]);
+  if (a.V > 512) return launch_small(small_sort_kernel<DT, 2>, kSmallSortSmem, a, s, &dev[1]);
+  return launch_small(small_sort_kernel<DT, 1>, kSmallSortSmem, a, s, &dev[0]);
+}
+
+template <int DT>
+cudaError_t launch_table_path(const ApplyArgs& a, cudaStream_t s) {
+  static thread_local int dev = -1;
+  return launch_small(small_table_kernel<DT>, kSmallTableSmem, a, s, &dev);
+}
+
+}  // namespace
+
+static_assert(kSortFlagOff + kSmallSortMaxV <= kSmallSortSmem, "sort kernel shared memory");
+static_assert(kBmassOff + (size_t)kTabBuckets * 8 <= kSmallTableSmem, "table kernel shared memory");
+
+cudaError_t launch_apply_small(topkp_dtype dt, const ApplyArgs& a, cudaStream_t s) {
+  if (a.V <= kSmallSortMaxV) {
+    switch (dt) {
+      case TOPKP_F32: return launch_sort_path<TOPKP_F32>(a, s);
+      case TOPKP_F16: return launch_sort_path<TOPKP_F16>(a, s);
+      case TOPKP_BF16: return launch_sort_path<TOPKP_BF16>(a, s);
+    }
+    return cudaErrorInvalidValue;
+  }
+  switch (dt) {
+    case TOPKP_F16: return launch_table_path<TOPKP_F16>(a, s);
+    case TOPKP_BF16: return launch_table_path<TOPKP_BF16>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace topkp
