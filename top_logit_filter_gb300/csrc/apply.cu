@@ -1580,6 +1580,59 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
       }
     };
 
+    // A sweep that reads q with the row: x and the q of two vectors per lane
+    // in flight together.  g(e, x, nv, qv, have_q) sees the vectors as in
+    // sweep(); qv holds the vector's q when have_q (16-byte aligned q rows;
+    // otherwise, and for the head and tail, g reads q itself).
+    const bool q16 = race_on && ((reinterpret_cast<uintptr_t>(qr + head) & 15u) == 0);
+    auto qsweep = [&](auto L_c, auto&& g) {
+      float qnone[VEC];
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) qnone[j] = 0.0f;
+      if (warp == 0 && own_head) {
+        const uint4 hq = load_partial(0, lane == 0 ? head : 0);
+        g(0, hq, lane == 0 ? head : 0, qnone, false);
+      }
+      constexpr int UQ = 2;
+      for (int s0 = 0; s0 < nsteps; s0 += UQ) {
+        uint4 xq[UQ];
+        float qv[UQ][VEC];
+#pragma unroll
+        for (int u = 0; u < UQ; ++u) {
+          const int v = wb + (s0 + u) * 32 + lane;
+          xq[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
+          if (v < we) xq[u] = load_vec(L_c, xv + v);
+#pragma unroll
+          for (int hq = 0; hq < VEC / 4; ++hq) {
+            float4 f = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (q16 && v < we) f = __ldg(reinterpret_cast<const float4*>(qr + head + v * VEC) + hq);
+            qv[u][4 * hq] = f.x;
+            qv[u][4 * hq + 1] = f.y;
+            qv[u][4 * hq + 2] = f.z;
+            qv[u][4 * hq + 3] = f.w;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < UQ; ++u) {
+          if (s0 + u < nsteps) {
+            const int v = wb + (s0 + u) * 32 + lane;
+            g(head + v * VEC, xq[u], v < we ? VEC : 0, qv[u], q16);
+          }
+        }
+      }
+      if (warp == kWarps - 1 && own_tail) {
+        const int et = head + nvec * VEC;
+        const uint4 tq = load_partial(et, lane == 0 ? tail : 0);
+        g(et, tq, lane == 0 ? tail : 0, qnone, false);
+      }
+    };
+    // race the kept elements (bits) of one vector
+    auto race_bits = [&](int e, const uint4& qin, uint32_t bits, const float (&qv)[VEC], bool have_q) {
+#pragma unroll
+      for (int j = 0; j < VEC; ++j)
+        if ((bits >> j) & 1u) race(t_of(vec_elem<DT>(qin, j)), have_q ? qv[j] : __ldg(qr + e + j), e + j);
+    };
+
     if (only_last) {
       // the last sorted position alone stays: find it, then write it
       if (h.fill) {
@@ -1641,6 +1694,17 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
         for (int u = 0; u < 4; ++u)
           if (k[u] && race_on) race(tq[u], qv[u], pos[u]);
       }
+    } else if (race_on && !minp_on) {
+      // every survivor of the filter races: one sweep reads q with the row
+      qsweep(ReadAs<kReadLast>{}, [&](int e, const uint4& qin, int nv, const float (&qv)[VEC], bool have_q) {
+        const uint32_t sb = survivor_bits(qin, nv);
+        uint32_t kb = 0;  // (min-p off still drops what is not >= -inf: a NaN)
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+          if (((sb >> j) & 1u) && t_of(vec_elem<DT>(qin, j)) >= lmp) kb |= 1u << j;
+        race_bits(e, qin, kb, qv, have_q);
+        if (nv != 0 && orow) write_vec(e, qin, nv, kb);
+      });
     } else {
       if (tid == 0) h.rcount = 0;
       __syncthreads();
@@ -1700,16 +1764,15 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
           }
         } else {
           // more candidates than the list holds: race them in a second sweep
+          // that reads q with the row
           seen = seen0;
-          sweep(Loads<kLoadsSimple>{}, ReadAs<kReadCg>{}, [&](int e, const uint4& qin, int nv) {
+          qsweep(ReadAs<kReadCg>{}, [&](int e, const uint4& qin, int nv, const float (&qv)[VEC], bool have_q) {
             const uint32_t sb = survivor_bits(qin, nv);
+            uint32_t kb = 0;
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) {
-              if ((sb >> j) & 1u) {
-                const float tj = t_of(vec_elem<DT>(qin, j));
-                if (tj >= lmp) race(tj, __ldg(qr + e + j), e + j);
-              }
-            }
+            for (int j = 0; j < VEC; ++j)
+              if (((sb >> j) & 1u) && t_of(vec_elem<DT>(qin, j)) >= lmp) kb |= 1u << j;
+            race_bits(e, qin, kb, qv, have_q);
           });
         }
       }

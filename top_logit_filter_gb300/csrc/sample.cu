@@ -251,6 +251,29 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleArgs a)
   float bsc = -INFINITY;
   int bidx = -1;
   auto t_of = [&](raw r) -> float { return fmaf(D::to_float(r), 1.4426950408889634f, nml); };
+  // the vector at e0 of a dense row with the elements of `drop` set to -inf:
+  // one 16-byte store when the output is aligned like the row
+  auto write_dropped = [&](int e0, const uint4& xin, uint32_t drop) {
+    if (vec_out) {
+      uint32_t w[4] = {xin.x, xin.y, xin.z, xin.w};
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        if ((drop >> j) & 1u) {
+          if (VEC == 8) {
+            const int sh = (j & 1) * 16;
+            w[j >> 1] = (w[j >> 1] & ~(0xffffu << sh)) | ((uint32_t)D::kNegInf << sh);
+          } else {
+            w[j] = (uint32_t)D::kNegInf;
+          }
+        }
+      }
+      st_global_hint(orow + e0, make_uint4(w[0], w[1], w[2], w[3]), pol_first);
+    } else {
+#pragma unroll
+      for (int j = 0; j < VEC; ++j)
+        if ((drop >> j) & 1u) orow[e0 + j] = D::kNegInf;
+    }
+  };
   // a candidate at an index above every one this thread has seen: it wins
   // ties (equal scores go to the larger index)
   auto race_next = [&](float t, float qv, int i) {
@@ -306,8 +329,54 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleArgs a)
     for (int i = tid; i < head; i += kThreads) visit(xr[i], i);
     // q of a whole vector in 16-byte loads when its row offset allows
     const bool qvec = qr != nullptr && ((reinterpret_cast<uintptr_t>(qr + head) & 15u) == 0);
+    // Rows whose kept elements are not rare (at least one in 16 of the
+    // listed ones, which are a sample of the row) read q with every vector,
+    // both in flight together; the others read q only for vectors that hold
+    // a kept element, after the vector has arrived.
+    bool dense_q = false;
+    if (qvec) {
+      unsigned long long kept = 0;
+      for (int t0 = tid; t0 < kListCap; t0 += kThreads) kept += t_of((raw)lraw[t0]) >= lmp ? 1u : 0u;
+      dense_q = block_sum(kept, ws) * 16 >= (unsigned long long)kListCap;
+    }
+    if (dense_q) {
+      constexpr int UQ = 2;
+      for (int v0 = tid; v0 < nvec; v0 += kThreads * UQ) {
+        uint4 xq[UQ];
+        float4 qq[UQ][VEC / 4];
+#pragma unroll
+        for (int u = 0; u < UQ; ++u) {
+          const int v = v0 + u * kThreads;
+          xq[u] = v < nvec ? ld_global_hint(xv + v, pol_first) : kNegVec;
+#pragma unroll
+          for (int hq = 0; hq < VEC / 4; ++hq)
+            qq[u][hq] = v < nvec ? __ldg(reinterpret_cast<const float4*>(qr + head + v * VEC) + hq)
+                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int u = 0; u < UQ; ++u) {
+          const int v = v0 + u * kThreads;
+          const int e0 = head + v * VEC;
+          uint32_t drop = 0;
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) {
+            const raw r = elem_of<DT>(xq[u], j);
+            if (r == D::kNegInf) continue;  // (also the padding past the row)
+            const float tj = t_of(r);
+            if (!(tj >= lmp)) {
+              drop |= 1u << j;
+            } else {
+              const float4 f = qq[u][j >> 2];
+              const float qj = (j & 3) == 0 ? f.x : (j & 3) == 1 ? f.y : (j & 3) == 2 ? f.z : f.w;
+              race_next(tj, qj, e0 + j);
+            }
+          }
+          if (drop && orow) write_dropped(e0, xq[u], drop);
+        }
+      }
+    }
     constexpr int U2 = 4;
-    for (int v0 = tid; v0 < nvec; v0 += kThreads * U2) {
+    for (int v0 = dense_q ? nvec : tid; v0 < nvec; v0 += kThreads * U2) {
       uint4 xq[U2];
 #pragma unroll
       for (int u = 0; u < U2; ++u) {
@@ -318,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleArgs a)
       for (int u = 0; u < U2; ++u) {
         const int v = v0 + u * kThreads;
         const int e0 = head + v * VEC;
-        uint32_t kb = 0;
+        uint32_t kb = 0, drop = 0;
         float t[VEC];
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
@@ -326,9 +395,10 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleArgs a)
           t[j] = t_of(r);
           if (r != D::kNegInf) {                 // never the -inf padding past the row
             if (t[j] >= lmp) kb |= 1u << j;
-            else if (orow) orow[e0 + j] = D::kNegInf;
+            else drop |= 1u << j;
           }
         }
+        if (drop && orow) write_dropped(e0, xq[u], drop);
         if (qr && kb) {
           float qv[VEC];
           if (qvec) {
