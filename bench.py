@@ -1,6 +1,7 @@
 """Benchmark: fused top-k / top-p filtering of B=256 x V=128256 bf16 logits.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--op filter|sample|sort|fused|v2] [--workload 1|2|3|4]
 
 One step = one topkp_apply call over the whole batch (joint top-k + top-p,
 workload 3: logits 2*N(0,1) in bf16, k ~ U{1..1024} with 10% of rows
@@ -15,7 +16,10 @@ kernel (read logits + write out = 4 bytes per element) per launch with the
 measured HBM copy bandwidth; `cpu_baseline` times the CPU oracle (test
 infrastructure, single-threaded numpy) on a bounded sample of the same rows;
 `e2e` runs the same calls from pinned host buffers with the copies inside the
-timed region.  `--impl reference` times that oracle alone as the reference
+timed region.  `--workload` times the filter on another of the five seeded
+configurations instead (1: 4 x 1024 fp32 joint, 2: 64 x 32000 fp16 top-p
+only, 4: 1024 x 151936 fp32 top-k only; the default is 3), with the same
+line; the committed ncu traffic applies to configuration 3 only.  `--impl reference` times that oracle alone as the reference
 arm (on rank 0; other ranks exit without work).
 """
 from __future__ import annotations
@@ -161,6 +165,16 @@ def _cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
+def _opt(a, b):
+    return None if a is None else a[b]
+
+
+def _mode_of(w) -> str:
+    if w["k"] is not None and w["p"] is not None:
+        return "joint top-k + top-p"
+    return "top-k only" if w["k"] is not None else "top-p only"
+
+
 def _cpu_baseline(w, budget_s: float, gpu_out=None):
     """The oracle as it stands, one row at a time, for about budget_s seconds.
     When the GPU's output of the same batch is given, the rows the oracle
@@ -170,11 +184,12 @@ def _cpu_baseline(w, budget_s: float, gpu_out=None):
     rows = 0
     infos = []
     while rows < w["B"] and (rows < 4 or time.perf_counter() - t0 < budget_s):
-        infos.append(O.apply_row(w["x"][rows], w["dtype"], w["p"][rows], int(w["k"][rows]))[1])
+        kk = _opt(w["k"], rows)
+        infos.append(O.apply_row(w["x"][rows], w["dtype"], _opt(w["p"], rows), None if kk is None else int(kk))[1])
         rows += 1
     dt = time.perf_counter() - t0
     line = {"value": rows / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {rows} rows of the B=256 x V=128256 bf16 workload, {dt:.1f} s, single-threaded numpy",
+            "sample": f"first {rows} rows of the B={w['B']} x V={w['V']} {w['dtype']} workload, {dt:.1f} s, single-threaded numpy",
             "host": {"cpu": _cpu_model(), "cpu_count": os.cpu_count()}}
     if gpu_out is not None:
         from parity import compare_row
@@ -235,11 +250,11 @@ def run_ours(args):
     from rawutil import raw_to_torch
     from top_logit_filter_gb300 import workloads
 
-    w = workloads.make(WORKLOAD)
+    w = workloads.make(args.workload)
     B, V, dt = w["B"], w["V"], w["dtype"]
     x = raw_to_torch(w["x"], dt, dev)
-    p = raw_to_torch(w["p"], dt, dev)
-    k = torch.from_numpy(w["k"]).to(dev)
+    p = raw_to_torch(w["p"], dt, dev) if w["p"] is not None else None
+    k = torch.from_numpy(w["k"]).to(dev) if w["k"] is not None else None
     out = torch.empty_like(x)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -276,34 +291,44 @@ def run_ours(args):
     value = _job_rows_per_s(ws, B, args.steps, total_s)
 
     # roofline of the filter kernel: one launch per step
-    alg_bytes = B * V * 2 * 2
+    esize = 4 if dt == "f32" else 2
+    alg_bytes = B * V * esize * 2
     kernel_s = total_s / args.steps / max(1, launches_per_step)
     achieved = alg_bytes / kernel_s / 1e9
     peak, peak_kind = _peak_hbm()
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": _traffic_per_launch(), "peak_source": f"{peak_kind} (copy bandwidth, burst)",
+                "traffic": _traffic_per_launch() if args.workload == WORKLOAD else None, "peak_source": f"{peak_kind} (copy bandwidth, burst)",
                 "algorithmic_bytes_per_launch": alg_bytes}
 
     # end to end through the public API from pinned host buffers
     hx = raw_to_torch(w["x"], dt).pin_memory()
-    hp = raw_to_torch(w["p"], dt).pin_memory()
-    hk = torch.from_numpy(w["k"]).pin_memory()
+    hp = raw_to_torch(w["p"], dt).pin_memory() if p is not None else None
+    hk = torch.from_numpy(w["k"]).pin_memory() if k is not None else None
     hout = torch.empty_like(hx).pin_memory()
     e2e_steps = max(3, min(50, args.steps))
-    dx, dp, dk = torch.empty_like(x), torch.empty_like(p), torch.empty_like(k)
-    for _ in range(2):
-        dx.copy_(hx, non_blocking=True); dp.copy_(hp, non_blocking=True); dk.copy_(hk, non_blocking=True)
+    dx = torch.empty_like(x)
+    dp = torch.empty_like(p) if p is not None else None
+    dk = torch.empty_like(k) if k is not None else None
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        if dp is not None:
+            dp.copy_(hp, non_blocking=True)
+        if dk is not None:
+            dk.copy_(hk, non_blocking=True)
         hout.copy_(tk.apply(dx, p=dp, k=dk), non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        dx.copy_(hx, non_blocking=True); dp.copy_(hp, non_blocking=True); dk.copy_(hk, non_blocking=True)
-        hout.copy_(tk.apply(dx, p=dp, k=dk), non_blocking=True)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_s = e0.elapsed_time(e1) / 1e3
-    h2d = hx.numel() * hx.element_size() + hp.numel() * hp.element_size() + hk.numel() * hk.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hp, hk) if t is not None)
     d2h = hout.numel() * hout.element_size()
     e2e_s = _max_over_ranks(e2e_s, ws, dev)
     e2e = {"value": _job_rows_per_s(ws, B, e2e_steps, e2e_s), "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -311,10 +336,12 @@ def run_ours(args):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+            "metric": METRIC if args.workload == WORKLOAD else
+                      f"rows/s and achieved HBM GB/s (% of peak), B={B} V={V} {dt} {_mode_of(w)}",
+            "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w["name"], "B": B, "V": V, "mode": "joint top-k + top-p",
+            "vs_baseline": None, "dtype": dt, "data": "synthetic",
+            "config": {"workload": w["name"], "B": B, "V": V, "mode": _mode_of(w),
                        "l2": "flushed before every timed step (512 MiB memset, outside the events)",
                        "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU",
                        "wall_s_timed_region": t_wall, "step_time": step_pct},
@@ -608,6 +635,8 @@ def main():
                     help="filter: the headline topkp_apply step; sample: the post-filter stage alone; "
                          "sort: the stable sort alone; fused: filter + min-p + sample in one call; "
                          "v2: the TopKTopPSampleV2 semantics")
+    ap.add_argument("--workload", type=int, choices=(1, 2, 3, 4), default=WORKLOAD,
+                    help="filter op only: which seeded configuration (3 is the headline batch)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing (profiling runs)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work for cpu_baseline")
     args = ap.parse_args()

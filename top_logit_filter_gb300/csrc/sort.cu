@@ -138,6 +138,18 @@ __global__ void __launch_bounds__(kThreads, 2) sort_kernel(const SortArgs a) {
       int32_t ix[kPer];
       uint32_t d[kPer], rk[kPer];
       const int wbase = t0 + warp * kWarpSpan;
+      {
+        // the next tile into L2 while this one is processed: values, then positions
+        const int n0 = t0 + kTile;
+        const int nv = min(kTile, V - n0);
+        if (nv > 0) {
+          const int vlines = (nv * (int)sizeof(raw) + 127) / 128;
+          const int ilines = pass == 0 ? 0 : (nv * 4 + 127) / 128;
+          if (tid < vlines) asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(sv + n0) + tid * 128));
+          else if (tid < vlines + ilines)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(si + n0) + (tid - vlines) * 128));
+        }
+      }
       // every load of the tile in flight before any is used
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
