@@ -31,8 +31,8 @@ def tk():
     return m
 
 
-def _both(tk, monkeypatch, x, dt, p, k):
-    monkeypatch.setenv("TOPKP_FORCE_PLAN", "small")
+def _both(tk, monkeypatch, x, dt, p, k, plan="small"):
+    monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
     a = _run_apply(tk, x, dt, p, k)
     monkeypatch.setenv("TOPKP_FORCE_PLAN", "c1")
     b = _run_apply(tk, x, dt, p, k)
@@ -64,24 +64,28 @@ def test_sort_path(tk, monkeypatch, dtype, V, mode):
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("V", [4097, 8191, 20000, 32000, 32768])
 @pytest.mark.parametrize("mode", ["k", "p", "kp"])
-def test_table_path(tk, monkeypatch, dtype, V, mode):
+@pytest.mark.parametrize("plan", ["small1", "small2"])
+def test_table_path(tk, monkeypatch, dtype, V, mode, plan):
+    """One CTA per row, and a cluster of two CTAs per row (each counts half
+    the row; the bucket sums, scans and tie ranks go through the cluster)."""
     rng = np.random.default_rng(V * 17 + len(mode))
     B = 9
     for kind in KINDS:
         x = _rows(rng, B, V, dtype, kind)
         k, p = _kp(rng, B, V, dtype, mode)
-        a, b = _both(tk, monkeypatch, x, dtype, p, k)
-        _same(a, b, dtype, f"{dtype} V={V} {mode} {kind}")
+        a, b = _both(tk, monkeypatch, x, dtype, p, k, plan)
+        _same(a, b, dtype, f"{plan} {dtype} V={V} {mode} {kind}")
         if kind in ("normal", "ties", "zeros"):
-            _check_all(a, x, dtype, p, k, f"table path {dtype} V={V} {mode} {kind}")
+            _check_all(a, x, dtype, p, k, f"table path {plan} {dtype} V={V} {mode} {kind}")
 
 
 @pytest.mark.parametrize("dtype", DTS)
 @pytest.mark.parametrize("V", [3001, 20011])
-def test_strided_unaligned_and_in_place(tk, monkeypatch, dtype, V):
+@pytest.mark.parametrize("plan", ["small1", "small2"])
+def test_strided_unaligned_and_in_place(tk, monkeypatch, dtype, V, plan):
     """Misaligned row starts, row strides above V, a separate misaligned
     output with untouched padding, and in place."""
-    monkeypatch.setenv("TOPKP_FORCE_PLAN", "small")
+    monkeypatch.setenv("TOPKP_FORCE_PLAN", plan)
     rng = np.random.default_rng(V)
     B = 5
     x = _rows(rng, B, V, dtype, "normal")

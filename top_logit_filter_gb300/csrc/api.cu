@@ -208,9 +208,13 @@ topkp_status apply_impl(const char* fn, const void* logits, int64_t B, int64_t V
   a.ldo = out ? ld_out : V;
   a.V = (int32_t)V;
   // Short rows take the on-chip kernels (small.cu) unless a plan of the main
-  // kernel is forced; "small" forces them wherever the shape allows.
+  // kernel is forced; "small" forces them wherever the shape allows, "small1"
+  // / "small2" with one CTA / a cluster of two per 16-bit row counted per key.
   const char* force = getenv("TOPKP_FORCE_PLAN");
-  const bool small = !fused && small_rows(dtype, V) && (!force || !*force || strcmp(force, "small") == 0);
+  const bool small = !fused && small_rows(dtype, V) && (!force || !*force || strncmp(force, "small", 5) == 0);
+  int table_cs = 2 * B <= (int64_t)sms ? 2 : 1;  // one CTA per SM: two per row while the batch fits
+  if (force && strcmp(force, "small1") == 0) table_cs = 1;
+  if (force && strcmp(force, "small2") == 0) table_cs = 2;
   const ApplyPlan plan = small ? ApplyPlan{} : plan_apply(B, V, k != nullptr, sms, force);
   a.cs = plan.cs;
   a.mixed = plan.mixed;
@@ -222,7 +226,7 @@ topkp_status apply_impl(const char* fn, const void* logits, int64_t B, int64_t V
   a.eps = eps;
   a.token = token;
   // cs CTAs per row; grid.x must stay below 2^31
-  const int64_t max_rows = INT_MAX / a.cs;
+  const int64_t max_rows = INT_MAX / (small ? 2 : a.cs);
   int launches = 0;
   for (int64_t r0 = 0; r0 < B; r0 += max_rows) {
     const int64_t nb = B - r0 < max_rows ? B - r0 : max_rows;
@@ -235,7 +239,7 @@ topkp_status apply_impl(const char* fn, const void* logits, int64_t B, int64_t V
     ai.min_p = min_p ? min_p + r0 : nullptr;
     ai.q = q ? q + r0 * ldq : nullptr;
     ai.token = token ? token + r0 : nullptr;
-    const cudaError_t e = small ? launch_apply_small(dtype, ai, (cudaStream_t)stream)
+    const cudaError_t e = small ? launch_apply_small(dtype, ai, table_cs, (cudaStream_t)stream)
                                 : launch_apply(dtype, ai, (cudaStream_t)stream);
     if (e != cudaSuccess) {
       cudaGetLastError();

@@ -71,11 +71,12 @@ ApplyPlan plan_apply(int64_t B, int64_t V, bool has_k, int num_sms, const char* 
 
 cudaError_t launch_apply(topkp_dtype dt, const ApplyArgs& a, cudaStream_t s);
 
-// Short rows (small.cu): one CTA per row holds the whole row on chip.  Rows
-// of at most kSmallSortMaxV elements (any dtype) are sorted in shared memory;
-// 16-bit rows of at most kSmallTableMaxV elements stay in registers and are
-// counted per key.  Same results as launch_apply, bit for bit; no cluster,
-// no fused sample.
+// Short rows (small.cu): the whole row stays on chip.  Rows of at most
+// kSmallSortMaxV elements (any dtype) are sorted in shared memory, one CTA
+// per row; 16-bit rows of at most kSmallTableMaxV elements stay in registers
+// and are counted per key, on one CTA per row or a cluster of table_cs = 2
+// (while two CTAs per row still fit one per SM).  Same results as
+// launch_apply, bit for bit; no fused sample.
 constexpr int kSmallSortMaxV = 4096;
 constexpr int kSmallTableMaxV = 32768;
 constexpr size_t kSmallHdrBytes = 512;
@@ -85,7 +86,7 @@ constexpr size_t kSmallTableSmem = kSmallHdrBytes + 65536 * 2 + 4096 * (4 + 8);
 inline bool small_rows(topkp_dtype dt, int64_t V) {
   return V <= kSmallSortMaxV || (dt != TOPKP_F32 && V <= kSmallTableMaxV);
 }
-cudaError_t launch_apply_small(topkp_dtype dt, const ApplyArgs& a, cudaStream_t s);
+cudaError_t launch_apply_small(topkp_dtype dt, const ApplyArgs& a, int table_cs, cudaStream_t s);
 
 // --------------------------------------------------------------- sorted
 struct SortedArgs {

@@ -21,6 +21,7 @@
 //     mass as count x mass(key).  The top-k threshold and the top-p cut follow
 //     from two block scans over the table in descending key order; ties of
 //     the cut are ranked by position from per-vector tie counts.
+#include "cluster.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -40,8 +41,10 @@ struct SmallHdr {
   uint32_t tkey;                      // cut key
   uint32_t r0;                        // ties of the cut key masked, in index order
   uint32_t kblock;                    // table kernel: block holding the top-k threshold
-  uint32_t wblk;                      // table kernel: block holding the top-p cut
+  uint32_t wblk;                      // table kernel: block the warp walk takes
+  uint32_t here;                      // table kernel: this CTA holds the block the walk takes
   unsigned long long wabove;          // table kernel: count or mass above the walked block
+  ClSlots cx;                         // table kernel: cluster exchange slots
 };
 
 // ------------------------------------------------------------ sort kernel
@@ -212,18 +215,31 @@ __device__ __forceinline__ uint32_t half_key(uint32_t w, int j) {
   return order_key<DT>((uint16_t)(j ? (w >> 16) : (w & 0xffffu)));
 }
 
-template <int DT>
+template <int DT, int CS>
 __global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   using D = DType<DT>;
   using raw = typename D::raw;
   static_assert(D::kKeyBits == 16, "16-bit keys");
+  static_assert(CS == 1 || CS == 2, "one CTA per row, or a cluster of two");
+  constexpr int VPT = kVecPerThread / CS;     // 16-byte vectors per thread
+  constexpr int NBH = kTabBuckets / CS;        // buckets of this CTA's key range
+  constexpr int BPB = NBH / kThreads;          // buckets per thread block of keys
+  constexpr int KPB = BPB * 16;                // keys per block
+  constexpr int KPL = KPB / 32;                // keys per lane in a warp walk
   SmallHdr& h = *reinterpret_cast<SmallHdr*>(smem);
   uint32_t* tab = reinterpret_cast<uint32_t*>(smem + kTabOff);
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const int64_t row = blockIdx.x;
+  // a cluster of CS CTAs per row: CTA r holds the r-th part of the row's
+  // elements and, for the scans, key range CS - 1 - r (the highest first)
+  const uint32_t rank = CS > 1 ? cluster_ctarank() : 0u;
+  const Clu cl{CS, rank};
+  int cph = 0;
+  const uint32_t peer = rank ^ 1u;
+  const uint32_t half = (uint32_t)(CS - 1) - rank;
+  const int64_t row = blockIdx.x / CS;
   const int V = a.V;
   const raw* xr = reinterpret_cast<const raw*>(a.x) + row * a.ldx;
   raw* orow = reinterpret_cast<raw*>(a.out) + row * a.ldo;
@@ -231,21 +247,23 @@ __global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArg
   const bool topk = a.k != nullptr && kv >= 1 && kv <= V - 1;
   const bool topp = a.p != nullptr;
   const bool in_place = reinterpret_cast<const void*>(xr) == reinterpret_cast<const void*>(orow);
-  if (!topk && !topp) {
+  if (!topk && !topp) {  // (the same in every CTA of the cluster: nothing shared was touched)
     if (!in_place)
-      for (int i = tid; i < V; i += kThreads) orow[i] = xr[i];
+      for (int i = (int)rank * kThreads + tid; i < V; i += CS * kThreads) orow[i] = xr[i];
     return;
   }
   const float thr = topp ? top_p_threshold<DT>(a.p, row) : 0.0f;
   const bool xvec = (reinterpret_cast<uintptr_t>(xr) & 15u) == 0;
   const bool ovec = (reinterpret_cast<uintptr_t>(orow) & 15u) == 0;
   const uint32_t NEG2 = (uint32_t)D::kNegInf * 0x10001u;
+  // this CTA's vector u: elements 8v .. 8v+7 with v = rank * VPT * kThreads + u * kThreads + tid
+  auto elem0 = [&](int u) -> int { return (((int)rank * VPT + u) * kThreads + tid) * 8; };
 
-  // ---- load: vector v = u * kThreads + tid holds elements 8v .. 8v+7 ----
-  uint4 q[kVecPerThread];
+  // ---- load ----
+  uint4 q[VPT];
 #pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) {
-    const int e = (u * kThreads + tid) * 8;
+  for (int u = 0; u < VPT; ++u) {
+    const int e = elem0(u);
     q[u] = make_uint4(NEG2, NEG2, NEG2, NEG2);
     if (e + 8 <= V && xvec) {
       asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -273,14 +291,15 @@ __global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArg
     h.part = 0;
     h.tkey = 0;
     h.r0 = 0;
+    h.here = 0;
   }
   __syncthreads();
 
-  // ---- per-key counts and the row max ----
+  // ---- per-key counts of this CTA's elements, and the row max ----
   uint32_t kmax = 0;
 #pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) {
-    const int e = (u * kThreads + tid) * 8;
+  for (int u = 0; u < VPT; ++u) {
+    const int e = elem0(u);
     const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -294,19 +313,38 @@ __global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArg
   kmax = __reduce_max_sync(0xffffffffu, kmax);
   if (lane == 0) atomicMax(&h.maxkey, kmax);
   __syncthreads();
-  const uint32_t maxkey = h.maxkey;
+  // (its cluster barrier also completes every CTA's table)
+  const uint32_t maxkey = (uint32_t)cl_reduce1<kClMax>(cl, h.cx, cph, h.maxkey);
   const MassRef mr(value_of_key<DT>(maxkey));
 
-  // ---- per 16-key bucket its count and (top-p) its mass; thread t takes
-  // buckets t, t + 512, ... so that the dense key ranges spread over all
-  // threads ----
+  // the row's count of a key: this CTA's table plus the peer's (two 16-bit
+  // counters per word; a count is at most 32768, so the halves never carry)
+  auto word_at = [&](int i) -> uint32_t {
+    uint32_t w = tab[i];
+    if (CS > 1) w += dsmem_ld_u32(dsmem_addr(tab + i, peer));
+    return w;
+  };
+  auto count_of = [&](uint32_t key) -> uint32_t {
+    const uint32_t w = word_at((int)(key >> 1));
+    return (key & 1u) ? (w >> 16) : (w & 0xffffu);
+  };
+
+  // ---- per 16-key bucket of this CTA's key range its count and (top-p)
+  // its mass; thread t takes buckets t, t + 512, ... so that the dense key
+  // ranges spread over all threads ----
   uint32_t* bcnt = reinterpret_cast<uint32_t*>(smem + kBcntOff);
   unsigned long long* bmass = reinterpret_cast<unsigned long long*>(smem + kBmassOff);
 #pragma unroll 2
-  for (int i = 0; i < kTabBuckets / kThreads; ++i) {
-    const int b = i * kThreads + tid;
-    const uint4 wa = reinterpret_cast<const uint4*>(tab)[2 * b];
-    const uint4 wb = reinterpret_cast<const uint4*>(tab)[2 * b + 1];
+  for (int i = 0; i < BPB; ++i) {
+    const int b = (int)half * NBH + i * kThreads + tid;
+    uint4 wa = reinterpret_cast<const uint4*>(tab)[2 * b];
+    uint4 wb = reinterpret_cast<const uint4*>(tab)[2 * b + 1];
+    if (CS > 1) {
+      const uint4 ra = dsmem_ld_v4(dsmem_addr(reinterpret_cast<const uint4*>(tab) + 2 * b, peer));
+      const uint4 rb = dsmem_ld_v4(dsmem_addr(reinterpret_cast<const uint4*>(tab) + 2 * b + 1, peer));
+      wa = make_uint4(wa.x + ra.x, wa.y + ra.y, wa.z + ra.z, wa.w + ra.w);
+      wb = make_uint4(wb.x + rb.x, wb.y + rb.y, wb.z + rb.z, wb.w + rb.w);
+    }
     const uint32_t ww[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
     uint32_t c = 0;
     unsigned long long m = 0;
@@ -326,31 +364,28 @@ __global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArg
     bmass[b] = m;
   }
   __syncthreads();
-  // ---- the table in descending key order: thread t owns the 128 keys
-  // (8 buckets) of block 511 - t ----
-  const uint32_t blk = (uint32_t)(kThreads - 1 - tid);
+  // ---- the table in descending key order: thread t owns the BPB buckets
+  // of block gblk (the highest blocks in the lowest threads, and the CTAs
+  // of lower rank hold the higher key ranges) ----
+  const uint32_t gblk = half * (uint32_t)kThreads + (uint32_t)(kThreads - 1 - tid);
   uint32_t cnt = 0;
   unsigned long long mass = 0;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    cnt += bcnt[blk * 8 + j];
-    mass += bmass[blk * 8 + j];
+  for (int j = 0; j < BPB; ++j) {
+    cnt += bcnt[gblk * BPB + j];
+    mass += bmass[gblk * BPB + j];
   }
-  auto count_of = [&](uint32_t key) -> uint32_t {
-    const uint32_t w = tab[key >> 1];
-    return (key & 1u) ? (w >> 16) : (w & 0xffffu);
-  };
   // Warp 0 walks block b down from its largest key, starting `above` from
   // the top: the first key at which above + the counts (or masses, keys >=
-  // lo only) so far reach `goal`.  Lane l takes keys b*128 + 127 - 4l - i.
+  // lo only) so far reach `goal`.  Lane l takes keys b*KPB + KPB-1 - KPL*l - i.
   // Every lane gets the key and the sum before it.
   auto warp_walk = [&](uint32_t b, unsigned long long above, unsigned long long goal, bool by_mass, uint32_t lo,
                        unsigned long long* before) -> uint32_t {
-    b &= (uint32_t)(kThreads - 1);  // a block of the table
-    unsigned long long v[4], s = 0;
+    b %= (uint32_t)(kThreads * CS);  // a block of the table
+    unsigned long long v[KPL], s = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t key = b * 128u + 127u - 4u * (uint32_t)lane - (uint32_t)i;
+    for (int i = 0; i < KPL; ++i) {
+      const uint32_t key = b * KPB + (KPB - 1) - KPL * (uint32_t)lane - (uint32_t)i;
       const uint32_t c = key >= lo ? count_of(key) : 0u;
       v[i] = by_mass ? (c ? (unsigned long long)c * mass_fixed(value_of_key<DT>(key), mr) : 0ull) : c;
       s += v[i];
@@ -367,9 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArg
     unsigned long long acc = above + incl - s;
     if (here) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < KPL; ++i) {
         if (acc + v[i] >= goal) {
-          key = b * 128u + 127u - 4u * (uint32_t)lane - (uint32_t)i;
+          key = b * KPB + (KPB - 1) - KPL * (uint32_t)lane - (uint32_t)i;
           break;
         }
         acc += v[i];
@@ -378,26 +413,47 @@ __global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArg
     *before = __shfl_sync(0xffffffffu, acc, f < 0 ? 0 : f);
     return __shfl_sync(0xffffffffu, key, f < 0 ? 0 : f);
   };
+  // a result of the CTA that walked, stored in every CTA of the cluster
+  auto put32 = [&](uint32_t* field, uint32_t v) {
+    *field = v;
+    if (CS > 1) dsmem_st_u32(dsmem_addr(field, peer), v);
+  };
+  auto put64 = [&](unsigned long long* field, unsigned long long v) {
+    *field = v;
+    if (CS > 1) dsmem_st_u64(dsmem_addr(field, peer), v);
+  };
+  // exclusive scan over the cluster in descending key order: the scan within
+  // the CTA plus the totals of the CTAs of lower rank
+  auto scan_desc = [&](unsigned long long v, unsigned long long* total) -> unsigned long long {
+    unsigned long long tot;
+    const unsigned long long ex = block_exclusive_scan(v, &tot, h.ws);
+    const unsigned long long t1[1] = {tot};
+    unsigned long long e1[1], a1[1];
+    cl_prefix<1>(cl, h.cx, cph, t1, e1, a1);
+    *total = a1[0];
+    return e1[0] + ex;
+  };
 
   // ---- top-k: the k-th largest key, from the counts above each block ----
   uint32_t kkey = 0;
   if (topk) {
     unsigned long long tot;
-    const unsigned long long above = block_exclusive_scan(cnt, &tot, h.ws);
+    const unsigned long long above = scan_desc(cnt, &tot);
     if (above < (unsigned long long)kv && (unsigned long long)kv <= above + cnt) {
-      h.kblock = blk;
+      h.wblk = gblk;
       h.wabove = above;
+      h.here = 1;
     }
     __syncthreads();
-    if (warp == 0) {
-      const uint32_t b = h.kblock;
+    if (h.here && warp == 0) {
+      const uint32_t b = h.wblk;
       unsigned long long before;
       const uint32_t key = warp_walk(b, h.wabove, (unsigned long long)kv, false, 0u, &before);
       unsigned long long part = 0;  // mass of the block's keys >= the threshold
       if (topp) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t kk = b * 128u + 127u - 4u * (uint32_t)lane - (uint32_t)i;
+        for (int i = 0; i < KPL; ++i) {
+          const uint32_t kk = b * KPB + (KPB - 1) - KPL * (uint32_t)lane - (uint32_t)i;
           const uint32_t c = kk >= key ? count_of(kk) : 0u;
           if (c) part += (unsigned long long)c * mass_fixed(value_of_key<DT>(kk), mr);
         }
@@ -405,16 +461,19 @@ __global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArg
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
       }
       if (lane == 0) {
-        h.kkey = key;
-        h.part = part;
+        put32(&h.kkey, key);
+        put32(&h.kblock, b);
+        put64(&h.part, part);
       }
     }
+    cl_sync(cl);
     __syncthreads();
     kkey = h.kkey;
+    if (tid == 0) h.here = 0;
     // survivors only: blocks below the threshold's block carry no mass, and
     // that block only its keys >= the threshold
-    if (blk < h.kblock) mass = 0;
-    else if (blk == h.kblock) mass = h.part;
+    if (gblk < h.kblock) mass = 0;
+    else if (gblk == h.kblock) mass = h.part;
   }
 
   // ---- top-p: the cut, walking down from the largest key; an element is
@@ -422,11 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArg
   uint32_t T = kkey, r0 = 0;
   if (topp) {
     unsigned long long S;
-    const unsigned long long above = block_exclusive_scan(mass, &S, h.ws);
+    const unsigned long long above = scan_desc(mass, &S);
     const unsigned long long R = S - mass_target(thr, S);
     if (R != 0 && above < R && R <= above + mass) {
-      h.wblk = blk;
+      h.wblk = gblk;
       h.wabove = above;
+      h.here = 1;
     }
     __syncthreads();
     if (R == 0) {
@@ -434,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArg
       T = maxkey;
       r0 = count_of(maxkey) - 1u;
     } else {
-      if (warp == 0) {
+      if (h.here && warp == 0) {
         unsigned long long base;
         const uint32_t key = warp_walk(h.wblk, h.wabove, R, true, kkey, &base);
         if (lane == 0) {
@@ -442,25 +502,26 @@ __global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArg
           // the (R - base) / u rounded up ties of largest positions stay
           const uint32_t c = count_of(key);
           const unsigned long long keep = u ? (R - base + u - 1) / u : (unsigned long long)c;
-          h.tkey = key;
-          h.r0 = c - (uint32_t)min(keep, (unsigned long long)c);
+          put32(&h.tkey, key);
+          put32(&h.r0, c - (uint32_t)min(keep, (unsigned long long)c));
         }
       }
+      cl_sync(cl);
       __syncthreads();
       T = h.tkey;
       r0 = h.r0;
     }
   }
 
-  // ---- ties of T ranked by position: index order is (u, thread, element) ----
-  uint32_t tie_before[kVecPerThread];
+  // ---- ties of T ranked by position: index order is (CTA, u, thread, element) ----
+  uint32_t tie_before[VPT];
 #pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) tie_before[u] = 0;
+  for (int u = 0; u < VPT; ++u) tie_before[u] = 0;
   if (r0 > 0) {
-    uint32_t tc[kVecPerThread];
+    uint32_t tc[VPT];
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      const int e = (u * kThreads + tid) * 8;
+    for (int u = 0; u < VPT; ++u) {
+      const int e = elem0(u);
       const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
       tc[u] = 0;
 #pragma unroll
@@ -470,38 +531,44 @@ __global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArg
     // four 16-bit lanes per word: at most 8 x kThreads ties per vector round
     unsigned long long pa = 0, pb = 0;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      pa |= (unsigned long long)tc[u] << (16 * u);
-      pb |= (unsigned long long)tc[u + 4] << (16 * u);
+    for (int u = 0; u < VPT; ++u) {
+      if (u < 4) pa |= (unsigned long long)tc[u] << (16 * u);
+      else pb |= (unsigned long long)tc[u] << (16 * (u - 4));
     }
     unsigned long long ea, eb, ta, tb;
     block_exclusive_scan2(pa, pb, &ea, &eb, &ta, &tb, h.ws);
-    uint32_t rounds = 0;  // ties in the earlier vector rounds
+    uint32_t rounds = 0;  // ties in the earlier vector rounds of this CTA
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
+    for (int u = 0; u < VPT; ++u) {
       const unsigned long long ex = u < 4 ? ea : eb, tot = u < 4 ? ta : tb;
       const int sh = 16 * (u & 3);
       tie_before[u] = rounds + (uint32_t)((ex >> sh) & 0xffffu);
       rounds += (uint32_t)((tot >> sh) & 0xffffu);
     }
+    // the CTAs before this one hold the earlier elements of the row
+    const unsigned long long t1[1] = {rounds};
+    unsigned long long e1[1], a1[1];
+    cl_prefix<1>(cl, h.cx, cph, t1, e1, a1);
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) tie_before[u] += (uint32_t)e1[0];
   }
 
   // ---- write: the element, or -inf, in original order ([guide] §2 step 8) ----
 #pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) {
-    const int e = (u * kThreads + tid) * 8;
+  for (int u = 0; u < VPT; ++u) {
+    const int e = elem0(u);
     if (e >= V) continue;
     const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
     uint32_t o[4];
-    uint32_t rank = tie_before[u];
+    uint32_t rnk = tie_before[u];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint32_t b = (j & 1) ? (wd[j >> 1] >> 16) : (wd[j >> 1] & 0xffffu);
       const uint32_t key = order_key<DT>((uint16_t)b);
       bool keep = key > T;
       if (key == T) {
-        keep = rank >= r0;
-        ++rank;
+        keep = rnk >= r0;
+        ++rnk;
       }
       const uint32_t ob = keep ? b : (uint32_t)D::kNegInf;
       if (j & 1) o[j >> 1] |= ob << 16;
@@ -515,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_table_kernel(const ApplyArg
         if (e + j < V) orow[e + j] = (raw)((j & 1) ? (o[j >> 1] >> 16) : (o[j >> 1] & 0xffffu));
     }
   }
+  cluster_fence_exit(cl);  // no peer reads this CTA's table or header any more
 }
 
 template <typename K>
@@ -541,9 +609,31 @@ cudaError_t launch_sort_path(const ApplyArgs& a, cudaStream_t s) {
 }
 
 template <int DT>
-cudaError_t launch_table_path(const ApplyArgs& a, cudaStream_t s) {
-  static thread_local int dev = -1;
-  return launch_small(small_table_kernel<DT>, kSmallTableSmem, a, s, &dev);
+cudaError_t launch_table_path(const ApplyArgs& a, int cs, cudaStream_t s) {
+  static thread_local int dev[2] = {-1, -1};
+  if (cs == 1) return launch_small(small_table_kernel<DT, 1>, kSmallTableSmem, a, s, &dev[0]);
+  // a cluster of two CTAs per row
+  auto kern = small_table_kernel<DT, 2>;
+  int d = 0;
+  cudaGetDevice(&d);
+  if (dev[1] != d) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallTableSmem);
+    if (e != cudaSuccess) return e;
+    dev[1] = d;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.B * 2));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmallTableSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace
@@ -551,7 +641,7 @@ cudaError_t launch_table_path(const ApplyArgs& a, cudaStream_t s) {
 static_assert(kSortFlagOff + kSmallSortMaxV <= kSmallSortSmem, "sort kernel shared memory");
 static_assert(kBmassOff + (size_t)kTabBuckets * 8 <= kSmallTableSmem, "table kernel shared memory");
 
-cudaError_t launch_apply_small(topkp_dtype dt, const ApplyArgs& a, cudaStream_t s) {
+cudaError_t launch_apply_small(topkp_dtype dt, const ApplyArgs& a, int table_cs, cudaStream_t s) {
   if (a.V <= kSmallSortMaxV) {
     switch (dt) {
       case TOPKP_F32: return launch_sort_path<TOPKP_F32>(a, s);
@@ -561,8 +651,8 @@ cudaError_t launch_apply_small(topkp_dtype dt, const ApplyArgs& a, cudaStream_t 
     return cudaErrorInvalidValue;
   }
   switch (dt) {
-    case TOPKP_F16: return launch_table_path<TOPKP_F16>(a, s);
-    case TOPKP_BF16: return launch_table_path<TOPKP_BF16>(a, s);
+    case TOPKP_F16: return launch_table_path<TOPKP_F16>(a, table_cs, s);
+    case TOPKP_BF16: return launch_table_path<TOPKP_BF16>(a, table_cs, s);
     default: return cudaErrorInvalidValue;
   }
 }
