@@ -98,7 +98,6 @@ struct __align__(16) ApplyHdr {
   int mt_qn;                             // mag clamped to >= floor; qn = bin of the negative floor;
   uint32_t mt_lump;                      // k0 = provisional max key; lump: floors hold zero-equal keys
   uint32_t slot;                         // block_first_true scratch
-  uint32_t rcount;                       // fused sample: race candidates listed
   ClSlots cx;                            // cluster exchange slots (rows split over a cluster)
 };
 static_assert(sizeof(ApplyHdr) <= kApplyHdrBytes, "header too large");
@@ -1483,12 +1482,6 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
       if (race_on) race(t, __ldg(qr + i), i);
       return true;
     };
-    // race candidates of the rows that are not listed: (position, t) pairs
-    // in the 64 KB region, free once the cut is known; raced four per thread
-    // at a time after the write sweep so that their q loads overlap
-    constexpr int kRaceCap = (int)(kApplyBigBytes / 8);
-    uint32_t* rpos = reinterpret_cast<uint32_t*>(big);
-    float* rt = reinterpret_cast<float*>(big + kApplyBigBytes / 2);
     const int myn = h.fill ? (int)h.nseg[warp] : 0;
     const uint32_t tcut = h.tie_cut;
     auto listed_survivor = [&](int j) -> bool {
@@ -1538,7 +1531,6 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
         seen = pre;
       }
     }
-    const unsigned long long seen0 = seen;  // a second sweep ranks the ties from the start again
     // bit j set when element j of the vector survives the filter
     auto survivor_bits = [&](const uint4& qin, int nv) -> uint32_t {
       uint32_t keep_ties = 0;
@@ -1694,8 +1686,9 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
         for (int u = 0; u < 4; ++u)
           if (k[u] && race_on) race(tq[u], qv[u], pos[u]);
       }
-    } else if (race_on && !minp_on) {
-      // every survivor of the filter races: one sweep reads q with the row
+    } else if (race_on) {
+      // the survivors that min-p keeps race in the write sweep itself, which
+      // reads q with the row (two vectors and their q in flight per lane)
       qsweep(ReadAs<kReadLast>{}, [&](int e, const uint4& qin, int nv, const float (&qv)[VEC], bool have_q) {
         const uint32_t sb = survivor_bits(qin, nv);
         uint32_t kb = 0;  // (min-p off still drops what is not >= -inf: a NaN)
@@ -1706,76 +1699,20 @@ __device__ __forceinline__ void apply_row(const ApplyArgs& a, const int64_t row,
         if (nv != 0 && orow) write_vec(e, qin, nv, kb);
       });
     } else {
-      if (tid == 0) h.rcount = 0;
-      __syncthreads();
+      // no race: the token is the last sorted position
       sweep(Loads<kLoadsSimple>{}, ReadAs<kReadLast>{}, [&](int e, const uint4& qin, int nv) {
         const uint32_t sb = survivor_bits(qin, nv);
         uint32_t kb = 0;
-        float tv[VEC];
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
-          tv[j] = 0.0f;
           if ((sb >> j) & 1u) {
             const raw r = vec_elem<DT>(qin, j);
             see_last(r, e + j);
-            tv[j] = t_of(r);
-            if (tv[j] >= lmp) kb |= 1u << j;
-          }
-        }
-        if (race_on) {
-          // list the kept elements: one warp scan, one shared atomic per warp
-          const uint32_t n = __popc(kb);
-          if (__any_sync(0xffffffffu, n != 0)) {
-            const uint32_t incl = warp_incl_scan(n);
-            uint32_t base = 0;
-            if (lane == 31) base = atomicAdd(&h.rcount, incl);
-            base = __shfl_sync(0xffffffffu, base, 31) + incl - n;
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) {
-              if ((kb >> j) & 1u) {
-                if (base < (uint32_t)kRaceCap) {
-                  rpos[base] = (uint32_t)(e + j);
-                  rt[base] = tv[j];
-                }
-                ++base;
-              }
-            }
+            if (t_of(r) >= lmp) kb |= 1u << j;
           }
         }
         if (nv != 0 && orow) write_vec(e, qin, nv, kb);
       });
-      if (race_on) {
-        __syncthreads();
-        const uint32_t nl = h.rcount;
-        if (nl <= (uint32_t)kRaceCap) {
-          for (uint32_t t0 = tid; t0 < nl; t0 += 4 * kThreads) {
-            float tq[4], qv[4];
-            int pos[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t j = t0 + u * kThreads;
-              pos[u] = j < nl ? (int)rpos[j] : -1;
-              tq[u] = j < nl ? rt[j] : 0.0f;
-              qv[u] = j < nl ? __ldg(qr + pos[u]) : 0.0f;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (pos[u] >= 0) race(tq[u], qv[u], pos[u]);
-          }
-        } else {
-          // more candidates than the list holds: race them in a second sweep
-          // that reads q with the row
-          seen = seen0;
-          qsweep(ReadAs<kReadCg>{}, [&](int e, const uint4& qin, int nv, const float (&qv)[VEC], bool have_q) {
-            const uint32_t sb = survivor_bits(qin, nv);
-            uint32_t kb = 0;
-#pragma unroll
-            for (int j = 0; j < VEC; ++j)
-              if (((sb >> j) & 1u) && t_of(vec_elem<DT>(qin, j)) >= lmp) kb |= 1u << j;
-            race_bits(e, qin, kb, qv, have_q);
-          });
-        }
-      }
     }
     if (a.token) {
       unsigned long long pick;
