@@ -97,12 +97,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_sort_kernel(const ApplyArgs
   }
   const float thr = topp ? top_p_threshold<DT>(a.p, row) : 0.0f;
 
-  int n = 1;
-  while (n < V) n <<= 1;
-  // thread t holds positions E t .. E t + E - 1 of the n entries, E = n / 512
-  // (at least 1; threads past n / E hold padding only, and their warps skip
-  // the compare stages)
-  const bool live = (tid >> 5) * 32 * E < n;  // warp-uniform
+  // thread t holds the entries of positions E t .. E t + E - 1 (before any
+  // sort: the row's elements in index order; E = the padded row / 512, at
+  // least 1); keep flags start cleared
   unsigned long long v[E];
 #pragma unroll
   for (int r = 0; r < E; ++r) {
@@ -111,93 +108,171 @@ __global__ void __launch_bounds__(kThreads, 1) small_sort_kernel(const ApplyArgs
     if (i < V) {
       const raw x = xr[i];
       rowv[i] = x;
+      keepf[i] = 0;
       v[r] = ((unsigned long long)order_key<DT>(x) << 32) | (unsigned long long)i;
     }
   }
-  // bitonic sort, ascending: (key, position) is the stable order.  A stage
-  // of stride s compares position i with i ^ s, ascending where i & size is
-  // 0: within a thread for s < E, between the lanes of a warp for s < 32 E,
-  // through shared memory beyond.
-  for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride >= 32 * E) {
+  // the largest entry: the max key and, of equal maxima, the largest
+  // position -- the last sorted position, which always survives
+  unsigned long long mx = 0;
 #pragma unroll
-        for (int r = 0; r < E; ++r) ent[tid * E + r] = v[r];
-        __syncthreads();
-        if (live) {
+  for (int r = 0; r < E; ++r)
+    if (tid * E + r < V) mx = max(mx, v[r]);
+  mx = block_max_u64(mx, h.ws);
+  const uint32_t maxkey = (uint32_t)(mx >> 32);
+  const int lastpos = (int)(uint32_t)mx;
+  const MassRef mr(value_of_key<DT>(maxkey));
+
+  // The k-th largest key by a radix select on 8-bit digits from the top (the
+  // key at sorted position V - k; ties of it survive).  ent is free until a
+  // sort needs it.
+  auto kth_largest = [&](int k) -> uint32_t {
+    uint32_t* hist = reinterpret_cast<uint32_t*>(ent);
+    uint32_t prefix = 0;
+    unsigned long long rank = (unsigned long long)k;
+    for (int l = 0; l < D::kKeyBits / 8; ++l) {
+      const int sh = D::kKeyBits - 8 * (l + 1);
+      if (tid < 256) hist[tid] = 0;
+      __syncthreads();
 #pragma unroll
-          for (int r = 0; r < E; ++r) {
-            const int i = tid * E + r;
-            const unsigned long long y = ent[i ^ stride];
-            const bool keep_min = ((i & size) == 0) == ((i & stride) == 0);
-            v[r] = keep_min ? min(v[r], y) : max(v[r], y);
-          }
+      for (int r = 0; r < E; ++r) {
+        if (tid * E + r < V) {
+          const uint32_t key = (uint32_t)(v[r] >> 32);
+          if (l == 0 || (key >> (sh + 8)) == prefix) atomicAdd(&hist[(key >> sh) & 255u], 1u);
         }
-        __syncthreads();
-      } else if (live) {
-        if (stride >= E) {
-          const int lm = stride / E;  // partner lane distance
+      }
+      __syncthreads();
+      // thread t < 256 holds digit 255 - t: a scan in descending digit order
+      const unsigned long long c = tid < 256 ? hist[255 - tid] : 0ull;
+      unsigned long long tot;
+      const unsigned long long above = block_exclusive_scan(c, &tot, h.ws);
+      if (tid < 256 && above < rank && rank <= above + c) {
+        h.kkey = (uint32_t)(255 - tid);
+        h.wabove = above;
+      }
+      __syncthreads();
+      prefix = (prefix << 8) | h.kkey;
+      rank -= h.wabove;
+      __syncthreads();
+    }
+    return prefix;
+  };
+  // bitonic sort of the first n entries (n a power of two), ascending:
+  // (key, position) is the stable order.  A stage of stride s compares
+  // position i with i ^ s, ascending where i & size is 0: within a thread
+  // for s < E, between the lanes of a warp for s < 32 E, through shared
+  // memory beyond.  Warps past n / E hold padding only and skip the stages.
+  auto sort_n = [&](int n) {
+    const bool live = (tid >> 5) * 32 * E < n;  // warp-uniform
+    for (int size = 2; size <= n; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        if (stride >= 32 * E) {
 #pragma unroll
-          for (int r = 0; r < E; ++r) {
-            const int i = tid * E + r;
-            const unsigned long long y = __shfl_xor_sync(0xffffffffu, v[r], lm);
-            const bool keep_min = ((i & size) == 0) == ((i & stride) == 0);
-            v[r] = keep_min ? min(v[r], y) : max(v[r], y);
+          for (int r = 0; r < E; ++r) ent[tid * E + r] = v[r];
+          __syncthreads();
+          if (live) {
+#pragma unroll
+            for (int r = 0; r < E; ++r) {
+              const int i = tid * E + r;
+              const unsigned long long y = ent[i ^ stride];
+              const bool keep_min = ((i & size) == 0) == ((i & stride) == 0);
+              v[r] = keep_min ? min(v[r], y) : max(v[r], y);
+            }
           }
-        } else {
-          if constexpr (E >= 8) {
-            if (stride == 4) sort_stage_in_thread<4, E>(v, tid, size);
-          }
-          if constexpr (E >= 4) {
-            if (stride == 2) sort_stage_in_thread<2, E>(v, tid, size);
-          }
-          if constexpr (E >= 2) {
-            if (stride == 1) sort_stage_in_thread<1, E>(v, tid, size);
+          __syncthreads();
+        } else if (live) {
+          if (stride >= E) {
+            const int lm = stride / E;  // partner lane distance
+#pragma unroll
+            for (int r = 0; r < E; ++r) {
+              const int i = tid * E + r;
+              const unsigned long long y = __shfl_xor_sync(0xffffffffu, v[r], lm);
+              const bool keep_min = ((i & size) == 0) == ((i & stride) == 0);
+              v[r] = keep_min ? min(v[r], y) : max(v[r], y);
+            }
+          } else {
+            if constexpr (E >= 8) {
+              if (stride == 4) sort_stage_in_thread<4, E>(v, tid, size);
+            }
+            if constexpr (E >= 4) {
+              if (stride == 2) sort_stage_in_thread<2, E>(v, tid, size);
+            }
+            if constexpr (E >= 2) {
+              if (stride == 1) sort_stage_in_thread<1, E>(v, tid, size);
+            }
           }
         }
       }
     }
-  }
-  if (tid == 0) {
-    h.maxkey = 0;
-    h.kkey = 0;
-  }
-  __syncthreads();
-  // the max (position V-1) and the k-th largest (position V-k; ties of it survive)
+  };
+
+  const uint32_t kkey = topk ? kth_largest(kv) : 0u;
+  if (topp && thr >= 1.0f) {
+    // masked wherever the cumulative mass is <= the whole mass: everything
+    // but the last sorted position
+    if (tid == 0) keepf[lastpos] = 1;
+  } else if (!topp || (!(thr > 0.0f) && isfinite(value_of_key<DT>(maxkey)))) {
+    // top-k alone, or top-p with threshold 0: masked where the cumulative
+    // mass is <= 0, that is the elements of zero mass (mass grows with the
+    // value), except the last sorted position; no order is needed
 #pragma unroll
-  for (int r = 0; r < E; ++r) {
-    const int j = tid * E + r;
-    if (j == V - 1) h.maxkey = (uint32_t)(v[r] >> 32);
-    if (topk && j == V - kv) h.kkey = (uint32_t)(v[r] >> 32);
-  }
-  __syncthreads();
-  const uint32_t maxkey = h.maxkey;
-  const uint32_t kkey = h.kkey;
-  const MassRef mr(value_of_key<DT>(maxkey));
-  unsigned long long m[E];
-  unsigned long long mine = 0;
-#pragma unroll
-  for (int r = 0; r < E; ++r) {
-    m[r] = 0;
-    const int j = tid * E + r;
-    if (topp && j < V) {
-      const uint32_t key = (uint32_t)(v[r] >> 32);
-      if (key >= kkey) m[r] = mass_fixed(value_of_key<DT>(key), mr);
-      mine += m[r];
+    for (int r = 0; r < E; ++r) {
+      const int i = tid * E + r;
+      if (i < V) {
+        const uint32_t key = (uint32_t)(v[r] >> 32);
+        const bool keep = key >= kkey && (!topp || mass_fixed(value_of_key<DT>(key), mr) > 0ull || i == lastpos);
+        keepf[i] = keep ? 1 : 0;
+      }
     }
-  }
-  unsigned long long S = 0, acc = 0;
-  if (topp) acc = block_exclusive_scan(mine, &S, h.ws);
-  const unsigned long long target = mass_target(thr, S);
+  } else {
+    // the cut needs the survivors in sorted order: with top-k only the
+    // elements >= the k-th largest (every other one has zero mass and stays
+    // masked), gathered to the first positions
+    int nc = V;
+    if (topk) {
+      uint32_t c = 0;
 #pragma unroll
-  for (int r = 0; r < E; ++r) {
-    const int j = tid * E + r;
-    if (j < V) {
-      const uint32_t key = (uint32_t)(v[r] >> 32);
-      acc += m[r];
-      // masked when the cumulative mass is <= the threshold, except the last position
-      const bool keep = key >= kkey && (!topp || acc > target || j == V - 1);
-      keepf[(uint32_t)v[r]] = keep ? 1 : 0;
+      for (int r = 0; r < E; ++r)
+        if (tid * E + r < V && (uint32_t)(v[r] >> 32) >= kkey) ++c;
+      unsigned long long tot;
+      uint32_t base = (uint32_t)block_exclusive_scan(c, &tot, h.ws);
+#pragma unroll
+      for (int r = 0; r < E; ++r)
+        if (tid * E + r < V && (uint32_t)(v[r] >> 32) >= kkey) ent[base++] = v[r];
+      __syncthreads();
+      nc = (int)tot;
+#pragma unroll
+      for (int r = 0; r < E; ++r) v[r] = tid * E + r < nc ? ent[tid * E + r] : ~0ull;
+      __syncthreads();
+    }
+    int n = 1;
+    while (n < nc) n <<= 1;
+    sort_n(n);
+    unsigned long long m[E];
+    unsigned long long mine = 0;
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+      m[r] = 0;
+      const int j = tid * E + r;
+      if (j < nc) {
+        const uint32_t key = (uint32_t)(v[r] >> 32);
+        if (key >= kkey) m[r] = mass_fixed(value_of_key<DT>(key), mr);
+        mine += m[r];
+      }
+    }
+    unsigned long long S;
+    unsigned long long acc = block_exclusive_scan(mine, &S, h.ws);
+    const unsigned long long target = mass_target(thr, S);
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+      const int j = tid * E + r;
+      if (j < nc) {
+        const uint32_t key = (uint32_t)(v[r] >> 32);
+        acc += m[r];
+        // masked when the cumulative mass is <= the threshold, except the last position
+        const bool keep = key >= kkey && (acc > target || j == nc - 1);
+        keepf[(uint32_t)v[r]] = keep ? 1 : 0;
+      }
     }
   }
   __syncthreads();
