@@ -128,3 +128,22 @@ def test_workload5_full_size(tk):
             kept_vals = O.decode(x[b], dtype)[bits(out[b], dtype) != NEG_INF[dtype]]
             assert (kept_vals >= kth).all(), b
         flipstats.record(f"workload 5 ({w['name']}, logits={'given' if with_logits else 'absent'})", w["B"], flips)
+
+
+def test_workload5_top_p_only_full_size(tk):
+    """The pre-sorted batch with top-k off: the top-p sum and cut run over the
+    whole sorted row (152064 elements), split over the rows' CTAs.  32 rows
+    element by element against the oracle, with and without logits."""
+    from top_logit_filter_gb300 import workloads
+    w = workloads.make(5)
+    dtype = w["dtype"]
+    rows = list(range(0, w["B"], w["B"] // 32))
+    x, sv, si, p = w["x"][rows], w["sorted_value"][rows], w["sorted_indices"][rows], w["p"][rows]
+    infos = [O.apply_sorted_row(sv[b], si[b], dtype, p[b], None)[1] for b in range(len(rows))]
+    for with_logits in (True, False):
+        out = _run_sorted(tk, sv, si, dtype, p, None, x if with_logits else None)
+        flips = 0
+        for b in range(len(rows)):
+            flips += compare_row(out[b], x[b], infos[b], dtype, where=f"wl5 top-p only logits={with_logits} row {b}")
+            _suffix_in_stable_order(out[b], x[b], dtype)
+        flipstats.record(f"workload 5 as top-p only (logits={'given' if with_logits else 'absent'})", len(rows), flips)

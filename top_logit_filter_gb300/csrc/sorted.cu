@@ -139,10 +139,40 @@ __global__ void __launch_bounds__(kThreads, 4) sorted_kernel(const SortedArgs a)
     const int per_cta = (tail + C - 1) / C;
     const int a0 = jk + min(tail, (int)crank * per_cta);
     const int a1 = jk + min(tail, ((int)crank + 1) * per_cta);
-    const int per_thr = (a1 - a0 + kThreads - 1) / kThreads;
-    const int t0 = min(a1, a0 + tid * per_thr), t1 = min(a1, t0 + per_thr);
-    unsigned long long mine = 0;
-    for (int j = t0; j < t1; ++j) mine += mass_fixed(D::to_float(sv[j]), m);
+    // Each thread sums a contiguous range of the tail in 16-byte loads: the
+    // ranges are whole vectors from the first 16-byte aligned position ia
+    // (thread 0 also takes [a0, ia), the last one the partial end).
+    const int ia = min(a1, a0 + (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(sv + a0) & 15u)) & 15u) / sizeof(raw)));
+    const int nvt = (a1 - ia) / VEC;                       // whole vectors from ia
+    const int per_thr = (nvt + kThreads - 1) / kThreads;   // vectors per thread
+    const int t0 = tid == 0 ? a0 : min(a1, ia + tid * per_thr * VEC);
+    const int t1 = tid == kThreads - 1 ? a1 : min(a1, ia + (tid + 1) * per_thr * VEC);
+    // mass of [s, e) (s on a vector boundary when it is >= ia), 4 vectors in flight
+    auto range_mass = [&](int s, int e) -> unsigned long long {
+      unsigned long long sum = 0;
+      int j = s;
+      for (; j < e && j < ia; ++j) sum += mass_fixed(D::to_float(sv[j]), m);
+      for (; j + 4 * VEC <= e; j += 4 * VEC) {
+        uint4 q[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) q[u] = __ldg(reinterpret_cast<const uint4*>(sv + j) + u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const raw* r = reinterpret_cast<const raw*>(&q[u]);
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) sum += mass_fixed(D::to_float(r[i]), m);
+        }
+      }
+      for (; j + VEC <= e; j += VEC) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(sv + j));
+        const raw* r = reinterpret_cast<const raw*>(&q);
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) sum += mass_fixed(D::to_float(r[i]), m);
+      }
+      for (; j < e; ++j) sum += mass_fixed(D::to_float(sv[j]), m);
+      return sum;
+    };
+    const unsigned long long mine = range_mass(t0, t1);
     const unsigned long long part = block_sum(mine, h.ws);
     if (tid == 0) {
       if (C > 1) {
