@@ -15,8 +15,9 @@ Prints one JSON line.  `roofline` compares the algorithmic bytes of the
 kernel (read logits + write out = 4 bytes per element) per launch with the
 measured HBM copy bandwidth; `cpu_baseline` times the CPU oracle (test
 infrastructure, single-threaded numpy) on a bounded sample of the same rows;
-`e2e` runs the same calls from pinned host buffers with the copies inside the
-timed region.  `--workload` times the filter on another of the five seeded
+`e2e` runs the same call from pinned host buffers with the copies inside the
+timed region (the batch pipelined in row chunks over three streams; the
+serial figure beside it).  `--workload` times the filter on another of the five seeded
 configurations instead (1: 4 x 1024 fp32 joint, 2: 64 x 32000 fp16 top-p
 only, 4: 1024 x 151936 fp32 top-k only; the default is 3), with the same
 line; the committed ncu traffic applies to configuration 3 only.  `--impl reference` times that oracle alone as the reference
@@ -233,6 +234,100 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+E2E_CHUNKS = 4
+
+
+def _e2e_filter(tk, w, dev, stream, x, p, k, out, args, ws):
+    """The filter end to end through the public API: each step copies the
+    batch's logits, p and k from pinned host memory, filters them and copies
+    the output back, all inside the timed region, and the next step starts
+    only when the output is on the host.  Two ways: serial (copy in, filter,
+    copy out on the caller's stream) and pipelined (the batch in E2E_CHUNKS
+    row chunks: copies in, filtering and copies out on three streams, so
+    that the two copy directions overlap).  `value` is the pipelined rate."""
+    import torch
+    from rawutil import raw_to_torch
+
+    B, dt = w["B"], w["dtype"]
+    hx = raw_to_torch(w["x"], dt).pin_memory()
+    hp = raw_to_torch(w["p"], dt).pin_memory() if p is not None else None
+    hk = torch.from_numpy(w["k"]).pin_memory() if k is not None else None
+    hout = torch.empty_like(hx).pin_memory()
+    steps = max(3, min(50, args.steps))
+    dx = torch.empty_like(x)
+    dp = torch.empty_like(p) if p is not None else None
+    dk = torch.empty_like(k) if k is not None else None
+    dout = torch.empty_like(x)
+
+    def serial_step():
+        dx.copy_(hx, non_blocking=True)
+        if dp is not None:
+            dp.copy_(hp, non_blocking=True)
+        if dk is not None:
+            dk.copy_(hk, non_blocking=True)
+        hout.copy_(tk.apply(dx, p=dp, k=dk, out=dout), non_blocking=True)
+
+    chunks = [(B * i // E2E_CHUNKS, B * (i + 1) // E2E_CHUNKS) for i in range(min(E2E_CHUNKS, B))]
+    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in chunks]
+    ev_run = [torch.cuda.Event() for _ in chunks]
+    ev_out = [torch.cuda.Event() for _ in chunks]
+
+    def piped_step():
+        s_in.wait_stream(stream)
+        with torch.cuda.stream(s_in):
+            # p and k whole (a few hundred bytes), then the logits chunk by chunk
+            if dp is not None:
+                dp.copy_(hp, non_blocking=True)
+            if dk is not None:
+                dk.copy_(hk, non_blocking=True)
+        for c, (r0, r1) in enumerate(chunks):
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_run[c])  # the last step's filter of this chunk has read its inputs
+                dx[r0:r1].copy_(hx[r0:r1], non_blocking=True)
+                ev_in[c].record(s_in)
+            with torch.cuda.stream(s_run):
+                s_run.wait_event(ev_in[c])
+                s_run.wait_event(ev_out[c])  # the last step's copy out of this chunk is done
+                tk.apply(dx[r0:r1], p=dp[r0:r1] if dp is not None else None, k=dk[r0:r1] if dk is not None else None,
+                         out=dout[r0:r1])
+                ev_run[c].record(s_run)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_run[c])
+                hout[r0:r1].copy_(dout[r0:r1], non_blocking=True)
+                ev_out[c].record(s_out)
+        stream.wait_stream(s_out)  # the step ends with its output on the host
+
+    def timed(step):
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return _max_over_ranks(e0.elapsed_time(e1) / 1e3, ws, dev)
+
+    def same_bits(a, b):
+        it = torch.int16 if a.element_size() == 2 else torch.int32
+        return torch.equal(a.view(it), b.view(it))
+
+    serial_s = timed(serial_step)
+    serial_ok = same_bits(hout, out.cpu())
+    hout.zero_()
+    piped_s = timed(piped_step)
+    piped_ok = same_bits(hout, out.cpu())
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hp, hk) if t is not None)
+    d2h = hout.numel() * hout.element_size()
+    return {"value": _job_rows_per_s(ws, B, steps, piped_s), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "pipeline": f"{len(chunks)} row chunks; copies in, filter and copies out on three streams",
+            "serial": {"value": _job_rows_per_s(ws, B, steps, serial_s), "unit": "rows/s"},
+            "output_matches_device_run": bool(serial_ok and piped_ok)}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -300,39 +395,7 @@ def run_ours(args):
                 "traffic": _traffic_per_launch() if args.workload == WORKLOAD else None, "peak_source": f"{peak_kind} (copy bandwidth, burst)",
                 "algorithmic_bytes_per_launch": alg_bytes}
 
-    # end to end through the public API from pinned host buffers
-    hx = raw_to_torch(w["x"], dt).pin_memory()
-    hp = raw_to_torch(w["p"], dt).pin_memory() if p is not None else None
-    hk = torch.from_numpy(w["k"]).pin_memory() if k is not None else None
-    hout = torch.empty_like(hx).pin_memory()
-    e2e_steps = max(3, min(50, args.steps))
-    dx = torch.empty_like(x)
-    dp = torch.empty_like(p) if p is not None else None
-    dk = torch.empty_like(k) if k is not None else None
-
-    def e2e_step():
-        dx.copy_(hx, non_blocking=True)
-        if dp is not None:
-            dp.copy_(hp, non_blocking=True)
-        if dk is not None:
-            dk.copy_(hk, non_blocking=True)
-        hout.copy_(tk.apply(dx, p=dp, k=dk), non_blocking=True)
-
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_s = e0.elapsed_time(e1) / 1e3
-    h2d = sum(t.numel() * t.element_size() for t in (hx, hp, hk) if t is not None)
-    d2h = hout.numel() * hout.element_size()
-    e2e_s = _max_over_ranks(e2e_s, ws, dev)
-    e2e = {"value": _job_rows_per_s(ws, B, e2e_steps, e2e_s), "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "steps": e2e_steps}
+    e2e = _e2e_filter(tk, w, dev, stream, x, p, k, out, args, ws)
 
     if rank == 0:
         line = {
