@@ -254,21 +254,30 @@ __global__ void __launch_bounds__(kThreads, 1) v2_topk_kernel(const V2Args a) {
   for (int j = tid; j < kV2MaxK; j += kThreads) s.list[j] = ~0ull;  // padding sorts last
   __syncthreads();
 
-  // ---- gather exactly k elements ----
+  // ---- gather exactly k elements (eight loads per lane in flight, the
+  // groups then taken in index order for the tie ranks) ----
   uint32_t seen = 0;
-  for (int base = wb; base < we; base += 32) {
-    const int i = base + lane;
-    uint32_t key = 0;
-    if (i < we) key = order_key<DT>(xr[i]);
-    const bool gt = i < we && key > T;
-    const bool eq = i < we && key == T;
-    const uint32_t be = __ballot_sync(0xffffffffu, eq);
-    const uint32_t r = tie_off + seen + __popc(be & ((1u << lane) - 1u));
-    seen += __popc(be);
-    if (gt || (eq && r < need_ties)) {
-      const uint32_t slot = atomicAdd(&s.ncol, 1u);
-      if (slot < (uint32_t)kV2MaxK)
-        s.list[slot] = ((unsigned long long)((~key) & KMASK) << 32) | (unsigned long long)(uint32_t)i;
+  for (int i0 = wb; i0 < we; i0 += 32 * 8) {
+    raw rv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * 32 + lane;
+      rv[u] = i < we ? xr[i] : (raw)0;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * 32 + lane;
+      const uint32_t key = i < we ? order_key<DT>(rv[u]) : 0u;
+      const bool gt = i < we && key > T;
+      const bool eq = i < we && key == T;
+      const uint32_t be = __ballot_sync(0xffffffffu, eq);
+      const uint32_t r = tie_off + seen + __popc(be & ((1u << lane) - 1u));
+      seen += __popc(be);
+      if (gt || (eq && r < need_ties)) {
+        const uint32_t slot = atomicAdd(&s.ncol, 1u);
+        if (slot < (uint32_t)kV2MaxK)
+          s.list[slot] = ((unsigned long long)((~key) & KMASK) << 32) | (unsigned long long)(uint32_t)i;
+      }
     }
   }
   __syncthreads();
@@ -342,41 +351,208 @@ __global__ void __launch_bounds__(kThreads, 1) v2_topk_kernel(const V2Args a) {
 
 // ------------------------------------------------- rows with top-k skipped
 // The row is already sorted (descending) in the workspace: sv / si.
+//
+// A whole row is up to 2^20 positions, and this GPU's FP64 pipe runs at a
+// sixty-fourth of the FP32 rate, so with logits the per-position work stays
+// in fp32 and integers:
+//   - S = sum of exp(x - max) as a fixed-point sum in units of 2^-43 (each
+//     term rounded to the nearest unit; the sum's error, about 1e-11, is far
+//     below the fp32 rounding of S that every probability uses);
+//   - the top-p prefix from fixed-point prefix sums of the fp32
+//     probabilities in units of 2^-63, found by three levels of search: the
+//     warps' sixteenths of the row, the sixteenths of the one that holds the
+//     cut, and one warp's walk through the last 1/256;
+//   - min-p compares each fp32 probability with the smallest fp32 at or above
+//     the fp64 threshold prob[0] * min_p, which decides exactly as the fp64
+//     comparison does;
+//   - the sample takes the largest fp32 ratio prob / (q + eps) first, and then
+//     forms the fp64 ratio only for the positions whose fp32 ratio lies within
+//     2^-20 of it: the fp32 ratio is within 2^-22 of the fp64 one, so the
+//     fp64 maximum, first on ties, is among them.
+// Rows of probabilities (input_is_logits false) take the general stages of
+// v2_cut.
+
+// Sum over this warp of a 64-bit value (every lane gets it).
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// The fp32 value of a float_order_key.
+__device__ __forceinline__ float float_of_order_key(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
+
+constexpr float kExpUnit = 8796093022208.0f;        // 2^43: units of exp(x - max) per 1
+constexpr float kProbUnit = 9223372036854775808.0f;  // 2^63: units of probability per 1
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 1) v2_sorted_kernel(const V2Args a) {
   using D = DType<DT>;
   using raw = typename D::raw;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   V2Shared& s = *reinterpret_cast<V2Shared*>(smem_raw);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.x;
   if (v2_topk_runs(a, row)) return;
   const int V = a.V;
   const raw* sv = reinterpret_cast<const raw*>(a.sv) + row * (int64_t)V;
   const int32_t* si = a.si + row * (int64_t)V;
   const float m = D::to_float(sv[0]);
-  // probabilities: exp(x - m) / S, S summed in fp64 from fp32 terms
-  double part = 0.0;
-  for (int j = tid; j < V; j += kThreads) {
-    const float v = D::to_float(sv[j]);
-    part += (double)(a.input_is_logits ? expf(v - m) : v);
-  }
-  const double S = block_sum_f64(part, s.wsd);
-  const float Sf = (float)S;
-  auto prob_of = [&](int j) -> float {
-    const float v = D::to_float(sv[j]);
-    return a.input_is_logits ? expf(v - m) / Sf : v;
-  };
   const float pv = a.p ? a.p[row] : 2.0f;
   const float mp = a.min_p ? a.min_p[row] : 0.0f;
   const float* qr = a.q ? a.q + row * a.ldq : nullptr;
-  const V2Cut c = v2_cut(V, false, pv, mp, qr != nullptr, prob_of, [&](int j) { return qr[j]; }, a.eps, s);
+  unsigned long long* wsu = reinterpret_cast<unsigned long long*>(s.wsd);
+  float Sf = 1.0f;
+  V2Cut c;
+  if (a.input_is_logits) {
+    // ---- S, and the probabilities exp(x - m) / S in fp32 ----
+    unsigned long long se = 0;
+#pragma unroll 8
+    for (int j = tid; j < V; j += kThreads) se += f2ull_rn(expf(D::to_float(sv[j]) - m) * kExpUnit);
+    Sf = (float)((double)block_sum(se, wsu) * (1.0 / 8796093022208.0));
+    auto prob_of = [&](int j) -> float { return expf(D::to_float(sv[j]) - m) / Sf; };
+    auto units = [&](int j) -> unsigned long long { return f2ull_rn(prob_of(j) * kProbUnit); };
+
+    // ---- top-p (mass of j and after > fp32(1 - p)): the first position
+    // whose exclusive prefix reaches T - thr ends the kept prefix ----
+    int n_topp = V;
+    if (pv < 1.0f) {
+      const float thr = __fsub_rn(1.0f, pv);
+      const unsigned long long thr_u = thr >= 1.0f ? ~0ull : f2ull_rn(thr * kProbUnit);
+      // level 1: the warps' sixteenths of the row
+      const int w1 = ((V + kWarps - 1) / kWarps + 31) & ~31;
+      const int a0 = min(V, warp * w1), a1 = min(V, a0 + w1);
+      unsigned long long part = 0;
+#pragma unroll 8
+      for (int j = a0 + lane; j < a1; j += 32) part += units(j);
+      part = warp_sum_u64(part);
+      unsigned long long T;
+      unsigned long long base = block_exclusive_scan(lane == 0 ? part : 0ull, &T, wsu);
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const unsigned long long target = T > thr_u ? T - thr_u : 0ull;
+      // the last range whose start lies below the target holds the first
+      // position reaching it (or that position is the range's end)
+      int lo = 0, hi = V;
+      unsigned long long lo_base = 0;
+      if (target > 0) {
+        if (lane == 0) s.wsi[warp] = base < target ? 1 : 0;
+        __syncthreads();
+        int wl = 0;
+        for (int w = 0; w < kWarps; ++w) wl = s.wsi[w] ? w : wl;
+        __syncthreads();
+        lo = min(V, wl * w1);
+        hi = min(V, lo + w1);
+        // the chosen range's start prefix, from the warp that owns it
+        if (warp == wl && lane == 0) wsu[kWarps - 1] = base;
+        __syncthreads();
+        lo_base = wsu[kWarps - 1];
+        __syncthreads();
+        // level 2: sixteenths of that range
+        const int w2 = ((hi - lo + kWarps - 1) / kWarps + 31) & ~31;
+        const int b0 = min(hi, lo + warp * w2), b1 = min(hi, b0 + w2);
+        unsigned long long part2 = 0;
+#pragma unroll 4
+        for (int j = b0 + lane; j < b1; j += 32) part2 += units(j);
+        part2 = warp_sum_u64(part2);
+        unsigned long long T2;
+        unsigned long long base2 = block_exclusive_scan(lane == 0 ? part2 : 0ull, &T2, wsu);
+        base2 = lo_base + __shfl_sync(0xffffffffu, base2, 0);
+        if (lane == 0) s.wsi[warp] = (base2 < target && b0 < b1) || warp == 0 ? 1 : 0;
+        __syncthreads();
+        int wl2 = 0;
+        for (int w = 0; w < kWarps; ++w) wl2 = s.wsi[w] ? w : wl2;
+        __syncthreads();
+        // level 3: one warp walks the chosen sixteenth, 32 positions at a time
+        if (warp == wl2) {
+          unsigned long long acc = base2;  // exclusive prefix at b0
+          int found = b1;                  // no position in [b0, b1) reaches the target: the end
+          for (int j0 = b0; j0 < b1; j0 += 32) {
+            const int j = j0 + lane;
+            const unsigned long long u = j < b1 ? units(j) : 0ull;
+            unsigned long long incl = u;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, j < b1 && acc + incl - u >= target);
+            if (hit) {
+              found = j0 + __ffs(hit) - 1;
+              break;
+            }
+            acc += __shfl_sync(0xffffffffu, incl, 31);
+          }
+          if (lane == 0) s.wsi[0] = found;
+        }
+        __syncthreads();
+        n_topp = s.wsi[0];
+        __syncthreads();
+      } else {
+        n_topp = 0;  // no position after the first keeps more than thr
+      }
+      n_topp = max(1, n_topp);
+    }
+
+    // ---- min-p: prob >= prob[0] * min_p (fp64) is prob >= its fp32 ceiling ----
+    c.minp_ran = mp > 0.0f;
+    int n_kept = n_topp;
+    if (c.minp_ran) {
+      if (mp >= 1.0f) {
+        n_kept = 1;
+      } else {
+        const float thd32 = __double2float_ru((double)prob_of(0) * (double)mp);
+        unsigned long long cnt = 0;
+#pragma unroll 8
+        for (int j = tid; j < n_topp; j += kThreads) cnt += (prob_of(j) >= thd32 || j == 0) ? 1u : 0u;
+        n_kept = (int)block_sum(cnt, wsu);
+      }
+    }
+    c.n_kept = max(1, n_kept);
+
+    // ---- the sample ----
+    c.pick = 0;
+    if (qr != nullptr) {
+      const float eps32 = a.eps;
+      uint32_t kmax = 0;
+#pragma unroll 4
+      for (int j = tid; j < c.n_kept; j += kThreads) kmax = max(kmax, float_order_key(prob_of(j) / (qr[j] + eps32)));
+      const float r32max = float_of_order_key((uint32_t)block_max_u64(kmax, wsu));
+      const float cut = r32max >= 0.0f ? r32max * (1.0f - 9.5367431640625e-7f) : r32max * (1.0f + 9.5367431640625e-7f);
+      double best = -1.0;
+      int bpos = -1;
+      for (int j = tid; j < c.n_kept; j += kThreads) {
+        const float pj = prob_of(j);
+        const float qj = qr[j];
+        if (pj / (qj + eps32) >= cut) {
+          const double r = (double)pj / ((double)qj + (double)eps32);
+          if (bpos < 0 || r > best) {
+            best = r;
+            bpos = j;
+          }
+        }
+      }
+      __syncthreads();  // every warp has read the maximum's scratch
+      c.pick = block_argmax_first(best, bpos, s.wsd, s.wsi);
+      if (c.pick < 0) c.pick = 0;
+    }
+  } else {
+    // probabilities given: the general stages
+    c = v2_cut(V, false, pv, mp, qr != nullptr, [&](int j) { return D::to_float(sv[j]); },
+               [&](int j) { return qr[j]; }, a.eps, s);
+  }
+  auto prob_out = [&](int j) -> float {
+    const float v = D::to_float(sv[j]);
+    return a.input_is_logits ? expf(v - m) / Sf : v;
+  };
 
   if (a.token && tid == 0) a.token[row] = si[c.pick];
   if (a.select) {
     const raw* xr = reinterpret_cast<const raw*>(a.x) + row * a.ldx;
     raw* orow = reinterpret_cast<raw*>(a.select) + row * a.ld_select;
     const raw def = a.input_is_logits ? D::kNegInf : (raw)0;
+#pragma unroll 8
     for (int i = tid; i < V; i += kThreads) orow[i] = def;
     __syncthreads();
     for (int j = tid; j < c.n_kept; j += kThreads) {
@@ -391,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) v2_sorted_kernel(const V2Args a) 
   if (a.sort_masked) {
     float* sm = a.sort_masked + row * (int64_t)V;
     const float fill = (c.minp_ran || !a.input_is_logits) ? 0.0f : -INFINITY;
-    for (int j = tid; j < V; j += kThreads) sm[j] = j < c.n_kept ? prob_of(j) : fill;
+    for (int j = tid; j < V; j += kThreads) sm[j] = j < c.n_kept ? prob_out(j) : fill;
   }
 }
 
