@@ -59,6 +59,17 @@ def test_sort_small_rows(tk, dtype, V):
     _check(x, dtype, sv, si, f"{dtype} V={V}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("B", [1, 20, 50, 100, 160])
+def test_sort_row_split_over_clusters(tk, dtype, B):
+    """Batches of 1 to 160 rows: the planner runs a row on a cluster of 8,
+    4, 2 or 1 CTAs (each counting its slice of every pass's source); the
+    result is the same stable sort."""
+    x = _rows(B, 5003, dtype, seed=B)
+    sv, si = _gpu_sort(tk, x, dtype)
+    _check(x, dtype, sv, si, f"{dtype} B={B}")
+
+
 @pytest.mark.parametrize("dtype", DTS)
 def test_sort_strided_rows(tk, dtype):
     x = _rows(3, 2053, dtype, seed=5)

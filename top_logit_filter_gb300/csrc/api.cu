@@ -437,7 +437,8 @@ topkp_status topkp_sort(const void* logits, int64_t B, int64_t V, int64_t ld_log
     return fail(TOPKP_ERR_PARAM_INVALID, "topkp_sort: outputs, workspace and logits must not overlap");
 
   int dev = 0;
-  if (current_sms(&dev) <= 0) return fail(TOPKP_ERR_LAUNCH, "topkp_sort: no usable CUDA device");
+  const int sms = current_sms(&dev);
+  if (sms <= 0) return fail(TOPKP_ERR_LAUNCH, "topkp_sort: no usable CUDA device");
 
   SortArgs a = {};
   a.x = logits;
@@ -447,7 +448,8 @@ topkp_status topkp_sort(const void* logits, int64_t B, int64_t V, int64_t ld_log
   a.ws_value = (char*)workspace + (n * 4 + 255) / 256 * 256;
   a.ldx = ld_logits;
   a.V = (int32_t)V;
-  const int64_t max_rows = INT_MAX;
+  a.cs = sort_cluster_size(B, sms);
+  const int64_t max_rows = INT_MAX / a.cs;
   int launches = 0;
   for (int64_t r0 = 0; r0 < B; r0 += max_rows) {
     const int64_t nb = B - r0 < max_rows ? B - r0 : max_rows;
@@ -547,6 +549,9 @@ topkp_status topkp_sample_v2(const void* logits, int64_t B, int64_t V, int64_t l
   sa.descending = 1;
   sa.skip_k = top_k;
   sa.skip_kmax = (int32_t)(V < ks_aligned ? V : ks_aligned);
+  // few rows skip top-k, so each is sorted by a cluster of eight CTAs (the
+  // clusters of the other rows leave at once)
+  sa.cs = B <= INT_MAX / 8 ? 8 : 1;
   cudaError_t e = launch_sort(dtype, sa, (cudaStream_t)stream);
   if (e != cudaSuccess) {
     cudaGetLastError();

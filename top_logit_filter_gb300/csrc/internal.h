@@ -147,7 +147,13 @@ struct SortArgs {
   int32_t descending;       // largest first (equal values still in increasing index)
   const int32_t* skip_k;    // [B] or nullptr: rows with 1 <= skip_k[row] <= skip_kmax are not sorted
   int32_t skip_kmax;
+  int32_t cs;               // CTAs per row (a thread-block cluster): 1, 2, 4 or 8
 };
+
+// CTAs per row of the sort for a batch of B rows on num_sms SMs: the
+// largest of 1, 2, 4, 8 that keeps the batch within one wave of two CTAs
+// per SM.
+int sort_cluster_size(int64_t B, int num_sms);
 
 cudaError_t launch_sort(topkp_dtype dt, const SortArgs& a, cudaStream_t s);
 

@@ -22,6 +22,7 @@
 #include <cstdio>
 #include <mutex>
 
+#include "cluster.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -67,7 +68,14 @@ __device__ __forceinline__ uint32_t scan256(uint32_t v, uint32_t* tmp) {
 
 }  // namespace
 
-template <int DT>
+// A row may also run on a thread-block cluster of CS CTAs, each owning a
+// contiguous slice of every pass's source: before each pass the CTAs count
+// that pass's digits in their slices and read one another's counts through
+// distributed shared memory, so each knows where its run of every digit
+// starts (the runs of the slices before it come first, which keeps the sort
+// stable); after each pass a fence and a cluster barrier make the pass's
+// writes visible to the whole cluster.  Few rows then still fill the GPU.
+template <int DT, int CS>
 __global__ void __launch_bounds__(kThreads, 2) sort_kernel(const SortArgs a) {
   using D = DType<DT>;
   using raw = typename D::raw;
@@ -76,12 +84,16 @@ __global__ void __launch_bounds__(kThreads, 2) sort_kernel(const SortArgs a) {
   SortShared& s = *reinterpret_cast<SortShared*>(sort_smem);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t row = blockIdx.x;
+  const uint32_t rank = CS > 1 ? cluster_ctarank() : 0u;
+  const int64_t row = blockIdx.x / CS;
   const int V = a.V;
   if (a.skip_k != nullptr) {
     const int kv = a.skip_k[row];
-    if (kv >= 1 && kv <= a.skip_kmax) return;  // a row the caller does not need sorted
+    if (kv >= 1 && kv <= a.skip_kmax) return;  // a row the caller does not need sorted (the whole cluster leaves)
   }
+  // this CTA's slice [s0, s1) of every pass's source
+  const int chunk = (V + CS - 1) / CS;
+  const int s0 = min(V, (int)rank * chunk), s1 = min(V, s0 + chunk);
   // descending: the keys inverted, so the stable ascending order of the
   // inverted keys is the largest value first with ties in index order
   const uint32_t kinv = a.descending ? (uint32_t)((1ull << D::kKeyBits) - 1ull) : 0u;
@@ -93,11 +105,12 @@ __global__ void __launch_bounds__(kThreads, 2) sort_kernel(const SortArgs a) {
   const uint32_t lt_mask = (1u << lane) - 1u;
   auto key_of = [&](raw r) -> uint32_t { return order_key<DT>(r) ^ kinv; };
 
-  // ---- every pass's digit counts from one read, scanned into bucket bases ----
+  // ---- every pass's digit counts from one read, scanned into bucket bases
+  // (one CTA per row; a cluster counts each pass's source before the pass) ----
   for (int i = tid; i < 4 * kDigits; i += kThreads) (&s.base[0][0])[i] = 0;
   for (int i = tid; i < kWarps * kDigits; i += kThreads) (&s.wcnt[0][0])[i] = 0;
   __syncthreads();
-  for (int i0 = 0; i0 < V; i0 += kTile) {
+  for (int i0 = 0; CS == 1 && i0 < V; i0 += kTile) {
     raw r[kPer];
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
@@ -121,6 +134,9 @@ __global__ void __launch_bounds__(kThreads, 2) sort_kernel(const SortArgs a) {
     if (tid < kDigits) s.base[p][tid] = ex;
   }
   __syncthreads();
+  // a cluster's later passes read what other SMs wrote in this launch:
+  // through L2 only, never a stale L1 line
+  auto ld_val = [&](const raw* p, int i, int pass) -> raw { return (pass == 0 || CS == 1) ? p[i] : __ldcg(p + i); };
 
   for (int pass = 0; pass < P; ++pass) {
     const int shift = 8 * pass;
@@ -130,10 +146,42 @@ __global__ void __launch_bounds__(kThreads, 2) sort_kernel(const SortArgs a) {
     int32_t* di = to_out ? out_i : ws_i;
     const raw* sv = pass == 0 ? xr : (to_out ? ws_v : out_v);
     const int32_t* si = to_out ? ws_i : out_i;  // unused in pass 0
+    if constexpr (CS > 1) {
+      // this pass's digit counts in this CTA's slice of the source, and the
+      // cluster's: a digit's run starts after the smaller digits' runs of the
+      // whole row and this digit's runs of the slices before this one
+      uint32_t* cnt = s.gstart;  // free until the tiles
+      if (tid < kDigits) cnt[tid] = 0;
+      __syncthreads();
+      for (int i0 = s0; i0 < s1; i0 += kThreads * kPer) {
+        raw r[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int i = i0 + u * kThreads + tid;
+          r[u] = i < s1 ? ld_val(sv, i, pass) : (raw)0;
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u)
+          if (i0 + u * kThreads + tid < s1) atomicAdd(&cnt[(key_of(r[u]) >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      cluster_sync_all();  // every CTA's counts are complete
+      uint32_t tot = 0, before = 0;
+      if (tid < kDigits) {
+        for (int r2 = 0; r2 < CS; ++r2) {
+          const uint32_t c = dsmem_ld_u32(dsmem_addr(cnt + tid, (uint32_t)r2));
+          tot += c;
+          before += (uint32_t)r2 < rank ? c : 0u;
+        }
+      }
+      const uint32_t ex = scan256(tot, s.tmp);
+      cluster_sync_all();  // no peer reads these counts any more
+      if (tid < kDigits) s.base[pass][tid] = ex + before;
+    }
     if (tid < kDigits) s.running[tid] = 0;
     __syncthreads();
 
-    for (int t0 = 0; t0 < V; t0 += kTile) {
+    for (int t0 = s0; t0 < s1; t0 += kTile) {
       raw r[kPer];
       int32_t ix[kPer];
       uint32_t d[kPer], rk[kPer];
@@ -141,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 2) sort_kernel(const SortArgs a) {
       {
         // the next tile into L2 while this one is processed: values, then positions
         const int n0 = t0 + kTile;
-        const int nv = min(kTile, V - n0);
+        const int nv = min(kTile, s1 - n0);
         if (nv > 0) {
           const int vlines = (nv * (int)sizeof(raw) + 127) / 128;
           const int ilines = pass == 0 ? 0 : (nv * 4 + 127) / 128;
@@ -156,15 +204,15 @@ __global__ void __launch_bounds__(kThreads, 2) sort_kernel(const SortArgs a) {
         const int i = wbase + u * 32 + lane;
         r[u] = 0;
         ix[u] = 0;
-        if (i < V) {
-          r[u] = sv[i];
-          ix[u] = pass == 0 ? i : si[i];
+        if (i < s1) {
+          r[u] = ld_val(sv, i, pass);
+          ix[u] = pass == 0 ? i : (CS == 1 ? si[i] : __ldcg(si + i));
         }
       }
       // ---- rank every element among the earlier equal digits of its warp ----
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
-        const bool valid = wbase + u * 32 + lane < V;
+        const bool valid = wbase + u * 32 + lane < s1;
         d[u] = valid ? (key_of(r[u]) >> shift) & 255u : 256u;  // 256: invalid lanes match only each other
         const uint32_t peers = __match_any_sync(0xffffffffu, d[u]);  // the lanes holding the same digit
         const uint32_t before = valid ? s.wcnt[warp][d[u]] : 0u;
@@ -207,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 2) sort_kernel(const SortArgs a) {
       }
       __syncthreads();
       // ---- each digit's run written to consecutive destination positions ----
-      const int tn = min(kTile, V - t0);
+      const int tn = min(kTile, s1 - t0);
       for (int L = tid; L < tn; L += kThreads) {
         const raw rv = (raw)s.stage_v[L];
         const uint32_t dd = (key_of(rv) >> shift) & 255u;
@@ -219,23 +267,55 @@ __global__ void __launch_bounds__(kThreads, 2) sort_kernel(const SortArgs a) {
       }
       __syncthreads();  // the stage is free for the next tile
     }
-    __syncthreads();  // this pass's writes before the next pass reads them
+    if constexpr (CS > 1) {
+      __threadfence();
+      cluster_sync_all();  // this pass's writes, by every CTA, before the next pass reads them
+    } else {
+      __syncthreads();  // this pass's writes before the next pass reads them
+    }
   }
 }
 
-template <int DT>
-static cudaError_t launch_sort_dt(const SortArgs& a, cudaStream_t s) {
+template <int DT, int CS>
+static cudaError_t launch_sort_cs(const SortArgs& a, cudaStream_t s) {
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
     const cudaError_t e =
-        cudaFuncSetAttribute(sort_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SortShared));
+        cudaFuncSetAttribute(sort_kernel<DT, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SortShared));
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  sort_kernel<DT><<<dim3((unsigned)a.B), dim3(kThreads), sizeof(SortShared), s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.B * CS));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sizeof(SortShared);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CS > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, sort_kernel<DT, CS>, a);
+}
+
+template <int DT>
+static cudaError_t launch_sort_dt(const SortArgs& a, cudaStream_t s) {
+  switch (a.cs) {
+    case 2: return launch_sort_cs<DT, 2>(a, s);
+    case 4: return launch_sort_cs<DT, 4>(a, s);
+    case 8: return launch_sort_cs<DT, 8>(a, s);
+    default: return launch_sort_cs<DT, 1>(a, s);
+  }
+}
+
+int sort_cluster_size(int64_t B, int num_sms) {
+  int cs = 1;
+  while (cs < 8 && B * (int64_t)(2 * cs) <= 2LL * num_sms) cs *= 2;
+  return cs;
 }
 
 cudaError_t launch_sort(topkp_dtype dt, const SortArgs& a, cudaStream_t s) {
@@ -311,7 +391,8 @@ extern "C" topkp_status topkp_sort_static(const void* logits, int64_t B, int64_t
   // set-up, once per device, with that device current: the scratch array's
   // device address (the symbol's host-side name is not one)
   int dev = -1;
-  if (device_sms(&dev) <= 0 || dev < 0 || dev >= 64)
+  const int sms = device_sms(&dev);
+  if (sms <= 0 || dev < 0 || dev >= 64)
     return report_error(TOPKP_ERR_LAUNCH, "topkp_sort_static: no usable CUDA device");
   void* scratch = nullptr;
   {
@@ -346,8 +427,9 @@ extern "C" topkp_status topkp_sort_static(const void* logits, int64_t B, int64_t
   a.ws_index = reinterpret_cast<int32_t*>(scratch);
   a.ws_value = static_cast<char*>(scratch) + (n * 4 + 255) / 256 * 256;
   a.ldx = ld_logits;
-  a.B = B;  // B * V fits the scratch, so B is far below the grid limit
+  a.B = B;  // B * V fits the scratch, so B * 8 is far below the grid limit
   a.V = (int32_t)V;
+  a.cs = sort_cluster_size(B, sms);
   const cudaError_t e = launch_sort(dtype, a, (cudaStream_t)stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
