@@ -7,8 +7,9 @@
 // A least-significant-digit radix sort per row on the order keys of
 // common.cuh (-0 and +0 share a key, so they stay in index order), 8-bit
 // digits: 2 passes for 16-bit keys, 4 for fp32.  One 512-thread CTA per
-// row.  The row is read once to count every pass's digits (P histograms of
-// 256 bins, scanned into bucket bases).  Then every pass walks its source in
+// row, or (small batches) a thread-block cluster of up to eight, described
+// at the kernel.  The row is read once to count every pass's digits (P
+// histograms of 256 bins, scanned into bucket bases).  Then every pass walks its source in
 // index order, 4096 elements per tile (eight per thread; warp w holds
 // elements w*256 .. w*256+255 of the tile, lanes consecutive): a warp ranks
 // each element among the earlier equal digits of its warp (one match_any finds
@@ -17,8 +18,8 @@
 // carries the earlier tiles, so every element lands at base + earlier tiles
 // + earlier warps + its rank in the warp: a stable counting sort on the
 // digit.  Passes alternate between the caller's workspace and the outputs
-// so that the last one writes the outputs.  Only CTA barriers, no waits;
-// every scatter position is checked against V.
+// so that the last one writes the outputs.  Only CTA and cluster barriers,
+// no waits; every scatter position is checked against V.
 #include <cstdio>
 #include <mutex>
 
