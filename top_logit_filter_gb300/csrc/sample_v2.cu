@@ -30,6 +30,18 @@ namespace topkp {
 namespace {
 
 constexpr int kV2MaxK = 1024;  // top-k never keeps more ([V2] TopK sampling: ks_max <= 1024)
+constexpr int kV2Cand = 4096;  // candidates of the single-bound top-k (above: the radix select)
+constexpr int kV2Bits = 12;    // bucket bits of the bound's histogram (4096 buckets)
+
+// Element j of a 16-byte vector of raw values.
+template <int DT>
+__device__ __forceinline__ typename DType<DT>::raw v2_elem(const uint4& q, int j) {
+  if (DType<DT>::kKeyBits == 16) {
+    const uint32_t w = (j & 4) ? ((j & 2) ? q.w : q.z) : ((j & 2) ? q.y : q.x);
+    return (typename DType<DT>::raw)((j & 1) ? (w >> 16) : (w & 0xffffu));
+  }
+  return (typename DType<DT>::raw)((j & 2) ? ((j & 1) ? q.w : q.z) : ((j & 1) ? q.y : q.x));
+}
 
 // Exclusive prefix sum of one double per thread over the CTA, in thread
 // order; *total gets the sum.  ws: kWarps doubles of shared scratch.
@@ -94,6 +106,7 @@ __device__ __forceinline__ int block_argmax_first(double v, int pos, double* wsv
 }
 
 struct V2Shared {
+  unsigned long long cand[kV2Cand];      // candidates of the single-bound top-k
   unsigned long long list[kV2MaxK];      // (inverted key << 32 | index), sorted ascending
   float prob[kV2MaxK];
   uint32_t whist[kWarps][256];           // per-warp digit counts
@@ -200,6 +213,127 @@ __global__ void __launch_bounds__(kThreads, 1) v2_topk_kernel(const V2Args a) {
   const int per = (V + kWarps - 1) / kWarps;
   const int wb = min(V, warp * per), we = min(V, wb + per);
 
+  // ---- single bound: the 16-byte vectors' maxima (and the unaligned head
+  // and tail elements) counted in 4096 buckets from the top of the key;
+  // the bucket holding the k-th largest of those is a lower bound L on the
+  // k-th largest element (k disjoint units reach it).  One more pass lists
+  // every element >= L, and a bitonic sort of the list gives the first k in
+  // order.  Too few units or too many candidates: the radix select below. ----
+  bool fast = false;
+  {
+    constexpr int VEC = 16 / (int)sizeof(raw);
+    uint32_t* hist = &s.whist[0][0];  // 4096 buckets
+    for (int i = tid; i < (1 << kV2Bits); i += kThreads) hist[i] = 0;
+    if (tid == 0) {
+      s.ncol = 0;
+      s.sel_digit = -1;
+    }
+    __syncthreads();
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(xr);
+    const int head = min(V, (int)(((16u - (uint32_t)(xa & 15u)) & 15u) / (uint32_t)sizeof(raw)));
+    const int nvec = (V - head) / VEC;
+    const int tail0 = head + nvec * VEC;
+    const uint4* xv = reinterpret_cast<const uint4*>(xr + head);
+    auto bucket_of = [&](uint32_t key) -> uint32_t { return key >> (KB - kV2Bits); };
+    for (int v0 = tid; v0 < nvec; v0 += kThreads * 4) {
+      uint4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + u * kThreads;
+        q[u] = v < nvec ? xv[v] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (v0 + u * kThreads < nvec) {
+          uint32_t km = 0;
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) km = max(km, order_key<DT>(v2_elem<DT>(q[u], j)));
+          atomicAdd(&hist[bucket_of(km)], 1u);
+        }
+      }
+    }
+    for (int i = tid; i < head; i += kThreads) atomicAdd(&hist[bucket_of(order_key<DT>(xr[i]))], 1u);
+    for (int i = tail0 + tid; i < V; i += kThreads) atomicAdd(&hist[bucket_of(order_key<DT>(xr[i]))], 1u);
+    __syncthreads();
+    // thread t holds buckets 8t .. 8t+7; the bucket where the count from the top reaches k
+    constexpr int BPT = (1 << kV2Bits) / kThreads;
+    unsigned long long c = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) c += hist[BPT * tid + j];
+    unsigned long long tot;
+    unsigned long long* wsu = reinterpret_cast<unsigned long long*>(s.wsd);
+    const unsigned long long pre = block_exclusive_scan(c, &tot, wsu);
+    const unsigned long long above = tot - pre - c;  // units in the buckets above this thread's
+    if (above < (unsigned long long)k && (unsigned long long)k <= above + c) {
+      unsigned long long acc = above;
+      for (int j = BPT - 1; j >= 0; --j) {
+        acc += hist[BPT * tid + j];
+        if (acc >= (unsigned long long)k) {
+          s.sel_digit = BPT * tid + j;
+          break;
+        }
+      }
+    }
+    __syncthreads();
+    const int lb = s.sel_digit;
+    if (lb >= 0) {
+      const uint32_t L = (uint32_t)lb << (KB - kV2Bits);
+      auto take = [&](raw r, int i) {
+        const uint32_t key = order_key<DT>(r);
+        if (key >= L) {
+          const uint32_t slot = atomicAdd(&s.ncol, 1u);
+          if (slot < (uint32_t)kV2Cand)
+            s.cand[slot] = ((unsigned long long)((~key) & KMASK) << 32) | (unsigned long long)(uint32_t)i;
+        }
+      };
+      for (int v0 = tid; v0 < nvec; v0 += kThreads * 4) {
+        uint4 q[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int v = v0 + u * kThreads;
+          q[u] = v < nvec ? xv[v] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int v = v0 + u * kThreads;
+          if (v < nvec) {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) take(v2_elem<DT>(q[u], j), head + v * VEC + j);
+          }
+        }
+      }
+      for (int i = tid; i < head; i += kThreads) take(xr[i], i);
+      for (int i = tail0 + tid; i < V; i += kThreads) take(xr[i], i);
+      __syncthreads();
+      const uint32_t n = s.ncol;
+      fast = n >= (uint32_t)k && n <= (uint32_t)kV2Cand;
+      if (fast) {
+        int n2 = 2;
+        while (n2 < (int)n) n2 <<= 1;
+        for (int j = (int)n + tid; j < n2; j += kThreads) s.cand[j] = ~0ull;  // padding sorts last
+        __syncthreads();
+        for (int size = 2; size <= n2; size <<= 1) {
+          for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t2 = tid; t2 < n2 / 2; t2 += kThreads) {
+              const int lo = 2 * t2 - (t2 & (stride - 1));
+              const int hi = lo + stride;
+              const bool up = (lo & size) == 0;
+              const unsigned long long x0 = s.cand[lo], x1 = s.cand[hi];
+              if ((x0 > x1) == up) {
+                s.cand[lo] = x1;
+                s.cand[hi] = x0;
+              }
+            }
+            __syncthreads();
+          }
+        }
+        for (int j = tid; j < kV2MaxK; j += kThreads) s.list[j] = j < k ? s.cand[j] : ~0ull;
+        __syncthreads();
+      }
+    }
+  }
+
+  if (!fast) {
   // ---- radix select of the k-th largest key, 8-bit digits from the top ----
   uint32_t prefix = 0;
   uint32_t rank = (uint32_t)k;  // rank of the wanted key among keys with this prefix, from the top
@@ -298,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) v2_topk_kernel(const V2Args a) {
       __syncthreads();
     }
   }
+  }  // radix select
 
   // ---- probabilities of the k positions ----
   auto value_at = [&](int j) -> float {
